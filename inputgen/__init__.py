@@ -1,0 +1,232 @@
+"""Seeded synthetic inputs for the attention-prefill workloads.
+
+This module is shared by the CUDA path's tests/benchmark and by the CPU
+oracle's tests.  It contains no attention arithmetic: only random number
+generation (``gen.c``), the workload shapes, conversions between bf16 bit
+patterns and wider floats, and the choice of sampled rows.
+
+Workload shapes follow the GPT-OSS attention layer the TokenSpeed-kernel
+pages benchmark (page "TokenSpeed-kernel: multi-silicon ...", section
+"Числа: Gluon на AMD MI355X": BF16 Q/K/V, head_dim 64, 64 query heads, 8 KV
+heads, full causal, sequence lengths 1K-8K, batch 1-16; sliding-window and
+attention-sink layers are named in the same section and in the ai-radar.it
+article, section "AMD MI355X: la prova sul campo").
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gen.c")
+_LIB = os.path.join(_HERE, "libinputgen.so")
+_lock = threading.Lock()
+_lib = None
+
+# Stream ids: every tensor of a workload draws from its own counter stream.
+STREAM_Q, STREAM_K, STREAM_V, STREAM_SINKS, STREAM_LENS, STREAM_ROWS = 1, 2, 3, 4, 5, 6
+
+
+def build_lib(force: bool = False) -> str:
+    """Compile gen.c into libinputgen.so next to it (plain gcc, portable C)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC,
+                               "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build_lib())
+            lib.ig_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
+                                           ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+            lib.ig_normal_bf16.restype = None
+            lib.ig_normal_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
+                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+            lib.ig_normal_f32.restype = None
+            lib.ig_uniform_int.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64]
+            lib.ig_uniform_int.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def normal_bf16(seed: int, stream: int, shape, mult: float = 1.0) -> np.ndarray:
+    """bf16 bit patterns (uint16) of fp32(N(0,1)) * mult, rounded to nearest even."""
+    out = np.empty(shape, dtype=np.uint16)
+    _load().ig_normal_bf16(seed, stream, mult, out.ctypes.data, out.size, _threads())
+    return out
+
+
+def normal_f32(seed: int, stream: int, shape, sigma: float = 1.0) -> np.ndarray:
+    out = np.empty(shape, dtype=np.float32)
+    _load().ig_normal_f32(seed, stream, sigma, out.ctypes.data, out.size, _threads())
+    return out
+
+
+def uniform_int(seed: int, stream: int, n: int, lo: int, hi: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.int32)
+    rc = _load().ig_uniform_int(seed, stream, lo, hi, out.ctypes.data, n)
+    if rc != 0:
+        raise ValueError("hi < lo")
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest even) and return the bit patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = np.isnan(x)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    r[nan] = 0x7FC0
+    return r
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    seqlens: list            # per-sequence lengths
+    Hq: int
+    Hkv: int
+    D: int
+    window: int              # <= 0: full causal
+    scale: float
+    q: np.ndarray            # uint16 bf16 bits [T, Hq, D]
+    k: np.ndarray            # uint16 bf16 bits [T, Hkv, D]
+    v: np.ndarray            # uint16 bf16 bits [T, Hkv, D]
+    sinks: np.ndarray | None  # float32 [Hq] or None
+    cu_seqlens: np.ndarray   # int32 [S+1]
+    seed: int
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seqlens)
+
+    def allowed_keys(self) -> int:
+        """Sum over (token) rows of the number of allowed keys, for one head."""
+        tot = 0
+        for L in self.seqlens:
+            t = np.arange(L, dtype=np.int64)
+            if self.window > 0:
+                tot += int(np.minimum(t + 1, self.window).sum())
+            else:
+                tot += int((t + 1).sum())
+        return tot
+
+    def unmasked_flops(self) -> float:
+        """4*D*Hq*sum|J|: the QK^T and PV multiply-adds of allowed pairs only."""
+        return 4.0 * self.D * self.Hq * self.allowed_keys()
+
+    def algorithmic_bytes(self) -> int:
+        """Read Q, K, V once; write out (bf16) and lse (fp32) once."""
+        T = self.total_tokens
+        return T * (2 * self.Hq * self.D * 2 + 2 * self.Hkv * self.D * 2 + 4 * self.Hq)
+
+
+def make(seqlens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, sink_sigma=1.0,
+         k_mult=1.0, with_sinks=True, name="custom") -> Workload:
+    seqlens = [int(x) for x in seqlens]
+    cu = np.zeros(len(seqlens) + 1, dtype=np.int32)
+    if seqlens:
+        cu[1:] = np.cumsum(np.asarray(seqlens, dtype=np.int64)).astype(np.int32)
+    T = int(cu[-1])
+    q = normal_bf16(seed, STREAM_Q, (T, Hq, D))
+    k = normal_bf16(seed, STREAM_K, (T, Hkv, D), k_mult)
+    v = normal_bf16(seed, STREAM_V, (T, Hkv, D))
+    sinks = normal_f32(seed, STREAM_SINKS, (Hq,), sink_sigma) if with_sinks else None
+    return Workload(name, seqlens, Hq, Hkv, D, window, scale, q, k, v, sinks, cu, seed)
+
+
+# The five configurations, smallest first.
+CONFIGS = {
+    "tiny_1x256_h4kv1": dict(desc="1 seq x 256 tokens, Hq=4, Hkv=1, D=64, sinks N(0,1), "
+                                  "scale 1/8, full causal"),
+    "causal_4x4096_h64kv8": dict(desc="4 seqs x 4096 tokens, Hq=64, Hkv=8, D=64, sinks N(0,1), "
+                                      "scale 1/8, full causal"),
+    "window128_4x4096_h64kv8": dict(desc="as causal_4x4096 with sliding window W=128"),
+    "ragged32_h64kv8": dict(desc="32 seqs, lengths U{512..8192} from the seed, Hq=64, Hkv=8, "
+                                 "sinks N(0,2), full causal"),
+    "ragged32_w128_h64kv8": dict(desc="ragged32 rerun with W=128"),
+    "long_1x32768_h64kv8": dict(desc="1 seq x 32768 tokens, K = bf16(3*N(0,1)), sinks N(0,1), "
+                                     "full causal"),
+}
+
+
+def ragged_lengths(seed: int, n: int = 32, lo: int = 512, hi: int = 8192):
+    return [int(x) for x in uniform_int(seed, STREAM_LENS, n, lo, hi)]
+
+
+def config(name: str, seed: int = 0) -> Workload:
+    if name == "tiny_1x256_h4kv1":
+        return make([256], 4, 1, seed=seed, name=name)
+    if name == "causal_4x4096_h64kv8":
+        return make([4096] * 4, 64, 8, seed=seed, name=name)
+    if name == "window128_4x4096_h64kv8":
+        return make([4096] * 4, 64, 8, window=128, seed=seed, name=name)
+    if name == "ragged32_h64kv8":
+        return make(ragged_lengths(seed), 64, 8, sink_sigma=2.0, seed=seed, name=name)
+    if name == "ragged32_w128_h64kv8":
+        return make(ragged_lengths(seed), 64, 8, window=128, sink_sigma=2.0, seed=seed, name=name)
+    if name == "long_1x32768_h64kv8":
+        return make([32768], 64, 8, k_mult=3.0, seed=seed, name=name)
+    raise KeyError(name)
+
+
+def sample_rows(w: Workload, n_target: int = 4096, seed_stream: int = STREAM_ROWS,
+                tile: int = 128):
+    """(token, head) rows covering every sequence and head, sequence ends,
+    q-tile boundaries, window edges; the rest uniform.  Returns (t int64, h int32)."""
+    rows = set()
+    cu = w.cu_seqlens
+    H = w.Hq
+    for s, L in enumerate(w.seqlens):
+        if L == 0:
+            continue
+        st = int(cu[s])
+        special = {0, L - 1}
+        for b in range(0, L, tile):
+            for off in (0, tile - 1):
+                if b + off < L:
+                    special.add(b + off)
+        if w.window > 0:
+            for off in (w.window - 1, w.window):
+                if off < L:
+                    special.add(off)
+        sp = sorted(special)
+        for i, off in enumerate(sp):
+            rows.add((st + off, (i * 7 + s) % H))
+        for h in range(H):
+            rows.add((st + sp[(h * 5 + s) % len(sp)], h))
+    T = w.total_tokens
+    need = max(0, n_target - len(rows))
+    if T > 0 and need > 0:
+        r = uniform_int(w.seed, seed_stream, 2 * need + 16, 0, T * H - 1)
+        for x in r:
+            rows.add((int(x) // H, int(x) % H))
+            if len(rows) >= n_target:
+                break
+    rows = sorted(rows)
+    t = np.array([r[0] for r in rows], dtype=np.int64)
+    h = np.array([r[1] for r in rows], dtype=np.int32)
+    return t, h
