@@ -1,0 +1,408 @@
+"""Benchmark of mha_prefill on GB300: unmasked TFLOP/s and tokens/s, % of the
+dense-BF16 tensor peak, roofline of the attention kernel, an end-to-end
+number through the C ABI with host buffers, and the CPU oracle as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...    # the CPU oracle as the reference arm
+
+One step = one tsk_mha_prefill call (scheduler pre-pass + attention kernel)
+over the whole workload, inputs resident in HBM.  L2 is flushed (a 256 MB
+write) before every timed step; only the step itself is inside the CUDA
+events.  Under torchrun (N > 1) every rank runs an independent replica on its
+own GPU (the operation has no cross-GPU exchange); value = all ranks' FLOPs /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputgen  # noqa: E402
+
+DEFAULT_WORKLOAD = "causal_4x4096_h64kv8"
+METRIC = "mha_prefill unmasked TFLOP/s and tokens/s on 1 GB300; % of dense-BF16 peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+NVSMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            def find(keys):
+                for k in keys:
+                    if k in d and isinstance(d[k], (int, float)):
+                        return float(d[k])
+                for v in d.values():
+                    if isinstance(v, dict):
+                        for k in keys:
+                            if k in v and isinstance(v[k], (int, float)):
+                                return float(v[k])
+                return None
+            bf = find(["bf16_tflops"])
+            if bf:
+                return {"bf16_tflops": bf,
+                        "bf16_tflops_sustained": find(["bf16_tflops_sustained"]) or bf,
+                        "hbm_gbs": find(["hbm_gbs"]) or FALLBACK_PEAKS["hbm_gbs"]}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gqa_attention_prefill_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """Per-launch DRAM bytes of the attention kernel from a committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(workload)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={NVSMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_rate(w, seconds_target, seed_stream=77):
+    """Times the CPU oracle on a uniform sample of (token, head) rows of `w`
+    sized for about `seconds_target` of CPU work.  Returns (flop/s, rows,
+    seconds, threads, flops)."""
+    import oracle
+    G = w.Hq // w.Hkv
+    T = w.total_tokens
+    cu = w.cu_seqlens
+
+    def rows_flops(n):
+        r = inputgen.uniform_int(w.seed, seed_stream + n, n, 0, T * w.Hq - 1)
+        t = (r // w.Hq).astype(np.int64)
+        h = (r % w.Hq).astype(np.int32)
+        s = np.searchsorted(cu, t, side="right") - 1
+        pos = t - cu[s]
+        nk = pos + 1 if w.window <= 0 else np.minimum(pos + 1, w.window)
+        return t, h, float(4.0 * w.D * nk.sum())
+
+    n = 2048
+    t, h, fl = rows_flops(n)
+    t0 = time.perf_counter()
+    _, _, thr = oracle.run_workload(w, rows=(t, h))
+    dt = time.perf_counter() - t0
+    n2 = int(min(4_000_000, max(n, n * seconds_target / max(dt, 1e-3))))
+    t, h, fl = rows_flops(n2)
+    t0 = time.perf_counter()
+    _, _, thr = oracle.run_workload(w, rows=(t, h))
+    dt = time.perf_counter() - t0
+    return fl / dt, n2, dt, thr, fl
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    w = inputgen.config(args.workload, seed=args.seed)
+    flops_total = w.unmasked_flops()
+    # each step: the oracle on a bounded row sample (~3 s of CPU work)
+    for _ in range(args.warmup):
+        oracle_rate(w, 0.5)
+    rates, secs, rows, thr = [], [], 0, 0
+    for _ in range(args.steps):
+        r, n, dt, thr, fl = oracle_rate(w, 3.0)
+        rates.append(r)
+        secs.append(dt)
+        rows = n
+    value = statistics.median(rates) / 1e12
+    ms_equiv = flops_total / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_equiv, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
+                   f"{len(w.seqlens)} seqs", "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "window": w.window, "note": "ms_per_step extrapolated from the sampled rate"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{rows} uniform (token, head) rows per step of {w.name}, "
+                                   f"~{statistics.median(secs):.1f} s each"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(inputgen.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", init_method="env://")
+    if args.impl == "reference":
+        rc = run_reference(args, ws, rank)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    from gqa_attention_prefill_gb300 import build as cuda_build
+    if not os.path.exists(pkg.library_path()):
+        cuda_build.build()
+    lib = pkg.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    w = inputgen.config(args.workload, seed=args.seed + rank)
+    T, Hq, Hkv, D = w.total_tokens, w.Hq, w.Hkv, w.D
+    flops = w.unmasked_flops()
+
+    # host (pinned) and device copies
+    h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_k = torch.from_numpy(w.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_v = torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_s = torch.from_numpy(w.sinks).pin_memory()
+    h_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
+    q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
+    sinks, cu = h_s.to(dev), h_cu.to(dev)
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(o=out, l=lse, qq=q, kk=k, vv=v, ss=sinks, cc=cu):
+        rc = pkg.tsk_mha_prefill(qq, kk, vv, ss, cc, w.num_seqs, T, Hq, Hkv, D, w.window,
+                                 w.scale, o, l, stream)
+        if rc != 0:
+            raise pkg.TskError(rc, "tsk_mha_prefill")
+
+    pkg.tsk_profile_enable(True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = pkg.tsk_get_device_status(stream)
+    if st != 0:
+        raise pkg.TskError(st, "device status after warm-up")
+
+    # ---------------------------------------------------------------- timed
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    attn_ms, pre_ms = [], []
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                      else local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+            a, b = pkg.tsk_profile_read()   # waits for this step's events
+            pre_ms.append(a)
+            attn_ms.append(b)
+        torch.cuda.synchronize()
+    barrier(ws)
+    step_ms = [s.elapsed_time(e) for s, e in ev]
+    st = pkg.tsk_get_device_status(stream)
+    if st != 0:
+        raise pkg.TskError(st, "device status after timed steps")
+    ms = reduce_max(sum(step_ms) / len(step_ms), ws)
+    attn_avg = reduce_max(sum(attn_ms) / len(attn_ms), ws)
+    value = flops * ws / (ms * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- end to end
+    h_out = torch.empty((T, Hq, D), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((T, Hq), dtype=torch.float32).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    d_s, d_cu = torch.empty_like(sinks), torch.empty_like(cu)
+    pkg.tsk_profile_enable(False)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_s.copy_(h_s, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        step(out, lse, d_q, d_k, d_v, d_s, d_cu)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(args.e2e_steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms.append(e0.elapsed_time(e1))
+    e2e_ms = reduce_max(sum(e_ms) / len(e_ms), ws)
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_s, h_cu))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    # the e2e outputs must equal the resident-input outputs
+    torch.cuda.synchronize()
+    same = torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, fp32 sinks)",
+        "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
+                   f"{len(w.seqlens)} seqs", "total_tokens": T, "Hq": Hq, "Hkv": Hkv, "D": D,
+                   "window": w.window, "scale": w.scale, "sinks": True, "lse": True,
+                   "l2": "flushed before every timed step (256 MB write)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "tokens_per_s": T * ws / (ms * 1e-3),
+        "pct_of_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
+        "unmasked_flop_per_step": flops,
+        "attention_kernel_ms": attn_avg, "prepass_kernel_ms": sum(pre_ms) / len(pre_ms),
+        "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        "roofline": {"bound": "tensor", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name),
+                     "peak_source": f"{peak_src} dense bf16 (burst)",
+                     "algorithmic_bytes": w.algorithmic_bytes(),
+                     "kernel": "attention_fwd_kernel"},
+        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "matches_resident_run": bool(same)},
+        "gpu_launches": args.steps * pkg.tsk_kernels_per_call(),
+        "clocks": clk.summary(),
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    if not args.no_cpu_baseline:
+        r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": r / 1e12, "unit": "TFLOP/s", "cores": thr,
+                                "kind": "oracle",
+                                "sample": f"{n} uniform (token, head) rows of {w.name} "
+                                          f"({fl / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+"""GB300 (sm_103a) mha_prefill: causal grouped-query attention with attention
+sinks and an optional sliding window over packed variable-length sequences.
+
+This package is a thin ctypes binding over the C ABI in ``include/tsk_mha.h``
+(library ``libtsk_mha.so``, built in-tree by ``build.py``).  It only marshals
+arguments: every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or fails to load, every call
+raises.
+
+The operation is the ``mha_prefill`` call of the TokenSpeed-kernel public API
+(README, section "Public API"), for the GPT-OSS attention layers described on
+page "TokenSpeed-kernel: multi-silicon ...", section "Числа: Gluon на AMD
+MI355X" (BF16, head_dim 64, 64 query / 8 KV heads, causal, sinks, sliding
+window).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["tsk_mha_prefill", "mha_prefill", "tsk_get_device_status", "tsk_status_string",
+           "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
+           "tsk_version", "TskError", "library_path", "load_library"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libtsk_mha.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "TSK_OK", -1: "TSK_ERR_INVALID_ARG", -2: "TSK_ERR_UNSUPPORTED",
+          -3: "TSK_ERR_ALIGNMENT", -4: "TSK_ERR_DEVICE", -5: "TSK_ERR_OOM", -6: "TSK_ERR_LAUNCH",
+          -7: "TSK_ERR_DEVICE_TIMEOUT", -8: "TSK_ERR_BAD_SEQLENS"}
+
+
+class TskError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({tsk_status_string(code)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads libtsk_mha.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: run __graft_entry__.build() "
+                               "(or python -m gqa_attention_prefill_gb300.build)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.tsk_mha_prefill.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32,
+                                        ctypes.c_float, P, P, P]
+        lib.tsk_mha_prefill.restype = ctypes.c_int
+        lib.tsk_status_string.argtypes = [ctypes.c_int]
+        lib.tsk_status_string.restype = ctypes.c_char_p
+        lib.tsk_get_device_status.argtypes = [P]
+        lib.tsk_get_device_status.restype = ctypes.c_int
+        lib.tsk_profile_enable.argtypes = [ctypes.c_int]
+        lib.tsk_profile_enable.restype = ctypes.c_int
+        lib.tsk_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_float)]
+        lib.tsk_profile_read.restype = ctypes.c_int
+        lib.tsk_kernels_per_call.argtypes = []
+        lib.tsk_kernels_per_call.restype = i32
+        lib.tsk_release.argtypes = []
+        lib.tsk_release.restype = ctypes.c_int
+        lib.tsk_debug_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.tsk_debug_set_wait_timeout_ns.restype = ctypes.c_int
+        lib.tsk_version.argtypes = []
+        lib.tsk_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def tsk_status_string(code: int) -> str:
+    try:
+        return load_library().tsk_status_string(code).decode()
+    except Exception:
+        return STATUS.get(code, str(code))
+
+
+def tsk_mha_prefill(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, Hq, Hkv, D, window,
+                    scale, out, lse, stream=None) -> int:
+    """Same arguments as the C function; tensors (or raw device addresses) for
+    the buffers, ``stream`` a torch.cuda.Stream / handle / None (current
+    stream).  Returns the status code (0 = TSK_OK)."""
+    lib = load_library()
+    return lib.tsk_mha_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens),
+                               int(num_seqs), int(total_tokens), int(Hq), int(Hkv), int(D),
+                               int(window), float(scale), _ptr(out), _ptr(lse),
+                               _stream_handle(stream))
+
+
+def mha_prefill(q, k, v, cu_seqlens, sinks=None, window: int = 0, scale: float | None = None,
+                out=None, lse=None, return_lse: bool = True, stream=None):
+    """Tensor-level convenience over ``tsk_mha_prefill``.
+
+    q: [T, Hq, 64] bf16 CUDA; k, v: [T, Hkv, 64] bf16 CUDA; cu_seqlens: int32
+    CUDA [num_seqs+1]; sinks: fp32 CUDA [Hq] or None.  Returns (out, lse) with
+    out [T, Hq, 64] bf16 and lse [T, Hq] fp32 (None if return_lse is False).
+    """
+    import torch
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if k.shape != (T, Hkv, D) or v.shape != (T, Hkv, D):
+        raise ValueError("k and v must be [T, Hkv, D] with q's T and D")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+    if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_cuda
+                              or sinks.numel() != Hq):
+        raise ValueError("sinks must be a float32 CUDA tensor of Hq elements")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    rc = tsk_mha_prefill(q, k, v, sinks, cu_seqlens, cu_seqlens.numel() - 1, T, Hq, Hkv, D,
+                         window, scale, out, lse if return_lse else None, stream)
+    if rc != 0:
+        raise TskError(rc, "tsk_mha_prefill")
+    return out, (lse if return_lse else None)
+
+
+def tsk_get_device_status(stream=None) -> int:
+    return load_library().tsk_get_device_status(_stream_handle(stream))
+
+
+def tsk_profile_enable(enable: bool = True) -> int:
+    return load_library().tsk_profile_enable(1 if enable else 0)
+
+
+def tsk_profile_read():
+    """(prepass_ms, attention_ms) of the last call made while profiling was on."""
+    a, b = ctypes.c_float(), ctypes.c_float()
+    rc = load_library().tsk_profile_read(ctypes.byref(a), ctypes.byref(b))
+    if rc != 0:
+        raise TskError(rc, "tsk_profile_read")
+    return a.value, b.value
+
+
+def tsk_debug_set_wait_timeout_ns(ns: int) -> int:
+    return load_library().tsk_debug_set_wait_timeout_ns(int(ns))
+
+
+def tsk_kernels_per_call() -> int:
+    return load_library().tsk_kernels_per_call()
+
+
+def tsk_release() -> int:
+    return load_library().tsk_release()
+
+
+def tsk_version() -> int:
+    return load_library().tsk_version()

@@ -1,0 +1,432 @@
+// Persistent, warp-specialised causal GQA attention forward for sm_103a.
+//
+// One CTA per SM walks a static stride over the work units of the sorted
+// query-tile list.  A unit is (query tile of 128 rows, KV head g, head pair):
+// two query heads of the same KV group over the same 128 tokens, so both
+// share every K/V tile staged in shared memory (GQA reuse) and have identical
+// key ranges.  Roles:
+//   warp 0        TMA producer: Q tiles (2 x 16 KB, double buffered) and a
+//                 ring of kStages K/V stages (16 KB + 16 KB each)
+//   warp 1        allocates TMEM; one lane issues tcgen05.mma:
+//                   S_t = Q_t K_j^T   (M=128, N=128, K=64, both K-major, smem)
+//                   O_t += P_t V_j    (M=128, N=64,  K=128; P from TMEM, V MN-major)
+//   warps 4..7    softmax + epilogue for query tile t=0 (one thread per row)
+//   warps 8..11   softmax + epilogue for query tile t=1
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+//               P0 [384,448) P1 [448,512)  (P is bf16, two per column)
+// The MMA warp computes S_t(j+1) while the softmax of tile t works on S_t(j),
+// and the two tiles interleave on the tensor core.
+//
+// Softmax (base 2): x = s * scale * log2(e).  The running maximum m and sum l
+// start from the sink (m = sink*log2 e, l = 1) or from (-inf, 0) without one.
+// The maximum used for exponentials is only raised when a tile's maximum
+// exceeds it by more than 8 (then O and l are rescaled); p <= 2^8 otherwise.
+// The result is exact up to rounding because the same m enters numerator and
+// denominator.  Only tiles that straddle the causal diagonal or the window's
+// lower edge evaluate the mask; tiles outside [kv_lo, diagonal] are never
+// visited.  Every wait is bounded (WaitCtl): on expiry the kernel records
+// TSK_ERR_DEVICE_TIMEOUT, stops all roles, drains its copies and MMAs, frees
+// TMEM and returns.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "schedule.cuh"
+
+namespace tsk {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 384;
+constexpr int kHeadDim = 64;
+constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // 16 KB (also K/V tiles)
+constexpr uint32_t kSmemQ = 0;                           // 2 buffers x 2 tiles
+constexpr uint32_t kSmemKV = 4 * kTileBytes;             // kStages x (K, V)
+constexpr uint32_t kSmemBar = kSmemKV + kStages * 2 * kTileBytes;
+constexpr uint32_t kSmemBytes = kSmemBar + 512 + 1024;   // barriers + slack for 1 KB alignment
+
+constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned long long kDrainTimeoutNs = 2000000000ull;  // in-flight work always finishes
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
+
+struct AttnParams {
+  const float* sinks;   // [Hq] or nullptr
+  __nv_bfloat16* out;   // [T, Hq, 64]
+  float* lse;           // [T, Hq] or nullptr
+  const int4* list;     // sorted query tiles (QTile)
+  const int* ws;        // ws[kWsNTiles] = number of query tiles
+  int* status;          // device status words
+  int Hq, Hkv, G, HP;   // HP = ceil(G / 2) head pairs per KV head
+  int window;
+  float scale_log2;     // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+// Barrier slots (8 bytes each) inside the barrier area.
+enum : int {
+  kBarQFull = 0,               // [2]
+  kBarQEmpty = 2,              // [2]
+  kBarKFull = 4,               // [kStages]
+  kBarVFull = 4 + kStages,     // [kStages]
+  kBarKVEmpty = 4 + 2 * kStages,
+  kBarSFull = 4 + 3 * kStages,  // [2]
+  kBarSFree = 6 + 3 * kStages,  // [2]
+  kBarPFull = 8 + 3 * kStages,  // [2]
+  kBarPVDone = 10 + 3 * kStages,  // [2]
+  kBarDrain = 12 + 3 * kStages,
+  kNumBars = 13 + 3 * kStages
+};
+
+// mbar_wait for warps whose every lane polls: the result is made warp-uniform
+// so that the warp-collective tcgen05 instructions that follow never diverge.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                               int site) {
+  const bool ok = mbar_wait(bar, parity, c, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct Unit {
+  int start, q0, kv_lo, len, n_kv, g, h0, ntiles;
+};
+
+__device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
+  const int per_tile = p.Hkv * p.HP;
+  const int qi = u / per_tile;
+  const int rem = u - qi * per_tile;
+  const int4 e = __ldg(p.list + qi);
+  Unit r;
+  r.start = e.x;
+  r.q0 = e.y;
+  r.kv_lo = e.z;
+  r.len = e.w;
+  r.n_kv = e.y / kTileM - e.z + 1;
+  r.g = rem / p.HP;
+  const int hp = rem - r.g * p.HP;
+  r.h0 = r.g * p.G + 2 * hp;
+  r.ntiles = (2 * hp + 1 < p.G) ? 2 : 1;
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kSmemBar;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemBar + 8 * kNumBars + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarQFull + i), 1);
+      mbar_init(bar(kBarQEmpty + i), 1);
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSFree + i), 4);
+      mbar_init(bar(kBarPFull + i), 4);
+      mbar_init(bar(kBarPVDone + i), 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarKVEmpty + s), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+  const int n_qtiles = p.ws[kWsNTiles];
+  const int total_units = n_qtiles * p.Hkv * p.HP;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t q_iter = 0, kv_iter = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        const int qb = q_iter & 1;
+        if (q_iter >= 2) ok = mbar_wait(bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, wc, 1);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kBarQFull + qb), w.ntiles * kTileBytes);
+        for (int t = 0; t < w.ntiles; ++t)
+          tma_load_3d(sbase + kSmemQ + (2 * qb + t) * kTileBytes, &tmQ, bar(kBarQFull + qb), 0,
+                      w.h0 + t, w.start + w.q0);
+        ++q_iter;
+        for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
+          const int s = kv_iter % kStages;
+          const uint32_t k = kv_iter / kStages;
+          if (k >= 1) ok = mbar_wait(bar(kBarKVEmpty + s), (k - 1) & 1, wc, 2);
+          if (!ok) break;
+          const int row = w.start + (w.kv_lo + j) * kTileN;
+          const uint32_t kdst = sbase + kSmemKV + s * 2 * kTileBytes;
+          mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
+          tma_load_3d(kdst, &tmK, bar(kBarKFull + s), 0, w.g, row);
+          mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
+          tma_load_3d(kdst + kTileBytes, &tmV, bar(kBarVFull + s), 0, w.g, row);
+        }
+      }
+      // Drain: wait for the last load issued into every buffer so that no
+      // copy is still in flight when the CTA exits (bounded, best effort).
+      WaitCtl dc = wc;
+      int dummy_abort = 0;
+      dc.abort_flag = &dummy_abort;
+      if (dc.timeout_ns < kDrainTimeoutNs) dc.timeout_ns = kDrainTimeoutNs;
+      for (uint32_t i = (kv_iter > kStages ? kv_iter - kStages : 0); i < kv_iter; ++i) {
+        mbar_wait(bar(kBarKFull + i % kStages), (i / kStages) & 1, dc, 11);
+        mbar_wait(bar(kBarVFull + i % kStages), (i / kStages) & 1, dc, 12);
+      }
+      for (uint32_t i = (q_iter > 2 ? q_iter - 2 : 0); i < q_iter; ++i)
+        mbar_wait(bar(kBarQFull + (i & 1)), (i >> 1) & 1, dc, 13);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t q_iter = 0, kv_iter = 0;
+      uint32_t s_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        const int qb = q_iter & 1;
+        ok = mbar_wait(bar(kBarQFull + qb), (q_iter >> 1) & 1, wc, 3);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qaddr = sbase + kSmemQ + 2 * qb * kTileBytes;
+        auto issue_s = [&](int t, int stage) {
+          const uint32_t a = qaddr + t * kTileBytes;
+          const uint32_t b = sbase + kSmemKV + stage * 2 * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            mma_ss(tmem + kColS0 + 128 * t, sdesc_sw128(a + 32 * kk), sdesc_sw128(b + 32 * kk),
+                   kIdescQK, kk > 0 ? 1u : 0u);
+          tc_commit(bar(kBarSFull + t));
+        };
+        auto issue_pv = [&](int t, int stage, bool acc) {
+          const uint32_t b = sbase + kSmemKV + stage * 2 * kTileBytes + kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts(tmem + kColO0 + 64 * t, tmem + kColP0 + 64 * t + 8 * kk,
+                   sdesc_sw128(b + 2048 * kk), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          tc_commit(bar(kBarPVDone + t));
+        };
+        // S_t(0)
+        {
+          const int s0 = kv_iter % kStages;
+          ok = mbar_wait(bar(kBarKFull + s0), (kv_iter / kStages) & 1, wc, 4);
+          if (!ok) break;
+          tc_fence_after();
+          for (int t = 0; t < w.ntiles && ok; ++t) {
+            if (s_cnt[t] > 0) ok = mbar_wait(bar(kBarSFree + t), (s_cnt[t] - 1) & 1, wc, 5);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(t, s0);
+            ++s_cnt[t];
+          }
+        }
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+          const uint32_t cur = kv_iter + j;
+          const int sc = cur % kStages;
+          const bool more = j + 1 < w.n_kv;
+          const int sn = (cur + 1) % kStages;
+          if (more) {
+            ok = mbar_wait(bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, wc, 6);
+            if (!ok) break;
+          }
+          ok = mbar_wait(bar(kBarVFull + sc), (cur / kStages) & 1, wc, 7);
+          if (!ok) break;
+          tc_fence_after();
+          for (int t = 0; t < w.ntiles; ++t) {
+            if (more) {
+              ok = mbar_wait(bar(kBarSFree + t), (s_cnt[t] - 1) & 1, wc, 5);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(t, sn);
+              ++s_cnt[t];
+            }
+            ok = mbar_wait(bar(kBarPFull + t), p_cnt[t] & 1, wc, 8);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, sc, j > 0);
+            ++p_cnt[t];
+          }
+          if (!ok) break;
+          tc_commit(bar(kBarKVEmpty + sc));
+        }
+        if (!ok) break;
+        kv_iter += w.n_kv;
+        tc_commit(bar(kBarQEmpty + qb));
+        ++q_iter;
+      }
+      // Make sure no MMA is still running before TMEM is freed.
+      tc_commit(bar(kBarDrain));
+      WaitCtl dc = wc;
+      int dummy_abort = 0;
+      dc.abort_flag = &dummy_abort;
+      if (dc.timeout_ns < kDrainTimeoutNs) dc.timeout_ns = kDrainTimeoutNs;
+      mbar_wait(bar(kBarDrain), 0, dc, 14);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;    // query tile of this warpgroup
+    const int wq = warp & 3;          // TMEM lane quarter
+    const int r = wq * 32 + lane;     // query row within the tile
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS0 + 128 * t;
+    const uint32_t tO = tmem + lane_base + kColO0 + 64 * t;
+    const uint32_t tP = tmem + lane_base + kColP0 + 64 * t;
+    const float sl2 = p.scale_log2;
+    uint32_t s_cnt = 0, pv_cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (t >= w.ntiles) continue;
+      const int h = w.h0 + t;
+      const int row = w.q0 + r;  // relative to sequence start
+      float m_used = -INFINITY, l = 0.f;
+      if (p.sinks) {
+        m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
+        l = 1.f;
+      }
+      for (int j = 0; j < w.n_kv; ++j) {
+        const int kt = w.kv_lo + j;
+        ok = mbar_wait_warp(bar(kBarSFull + t), s_cnt & 1, wc, 9);
+        if (!ok) break;
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld_32x32b_x32(tS + 0, sr + 0);
+        tmem_ld_32x32b_x32(tS + 32, sr + 32);
+        tmem_ld_32x32b_x32(tS + 64, sr + 64);
+        tmem_ld_32x32b_x32(tS + 96, sr + 96);
+        tmem_wait_ld();
+        reg_fence<128>(sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSFree + t));
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        const int kbase = kt * kTileN;
+        const bool edge = (kbase + kTileN - 1 > w.q0) ||
+                          (p.window > 0 && kbase < w.q0 + kTileM - p.window);
+        if (edge) {
+          const int hi_c = row - kbase;
+          const int lo_c = p.window > 0 ? row - p.window + 1 - kbase : -1;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > hi_c || c < lo_c) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_tile = mx * sl2;
+        float alpha = 1.f;
+        const bool need = m_tile > m_used + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          if (m_tile > m_used) {
+            alpha = ex2_approx(m_used - m_tile);  // m_used = -inf gives 0
+            m_used = m_tile;
+          }
+        }
+        l *= alpha;
+        const float m_use = m_used == -INFINITY ? 0.f : m_used;
+        uint32_t pk[64];
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
+          rs += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l += rs;
+        if (j > 0) {
+          // O_t is stable and P_t reusable once PV_t(j-1) has completed.
+          ok = mbar_wait_warp(bar(kBarPVDone + t), pv_cnt & 1, wc, 10);
+          if (!ok) break;
+          ++pv_cnt;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            uint32_t o[64];
+            tmem_ld_32x32b_x32(tO, o);
+            tmem_ld_32x32b_x32(tO + 32, o + 32);
+            tmem_wait_ld();
+            reg_fence<64>(o);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st_32x32b_x32(tO, o);
+            tmem_st_32x32b_x32(tO + 32, o + 32);
+          }
+        }
+        tmem_st_32x32b_x32(tP, pk);
+        tmem_st_32x32b_x32(tP + 32, pk + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPFull + t));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      ok = mbar_wait_warp(bar(kBarPVDone + t), pv_cnt & 1, wc, 10);
+      if (!ok) break;
+      ++pv_cnt;
+      tc_fence_after();
+      uint32_t o[64];
+      tmem_ld_32x32b_x32(tO, o);
+      tmem_ld_32x32b_x32(tO + 32, o + 32);
+      tmem_wait_ld();
+      reg_fence<64>(o);
+      if (row < w.len) {
+        const float inv = 1.f / l;
+        const size_t orow = (size_t)(w.start + row) * p.Hq + h;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+          dst[c] = v;
+        }
+        if (p.lse) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+      }
+      tc_fence_before();
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tsk

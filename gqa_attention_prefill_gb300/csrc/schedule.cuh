@@ -1,0 +1,147 @@
+// Varlen scheduler pre-pass: one CTA turns cu_seqlens into the list of query
+// tiles (128 query rows of one sequence), each with its key-tile range, sorted
+// by cost (number of key tiles) in descending order, so that the persistent
+// attention kernel hands out the longest work first (longest-processing-time
+// order).  It also checks cu_seqlens: cu[0] == 0, non-decreasing,
+// cu[num_seqs] == total_tokens; on failure it records TSK_ERR_BAD_SEQLENS and
+// publishes an empty list.
+#pragma once
+#include <cstdint>
+
+namespace tsk {
+
+constexpr int kSchedThreads = 1024;
+constexpr int kCostBins = 4096;  // costs >= kCostBins share the top bin
+constexpr int kTileM = 128;      // query rows per tile
+constexpr int kTileN = 128;      // keys per tile
+
+// Workspace words (int32) at the head of the per-stream workspace.
+constexpr int kWsStatus = 0;   // [0] error code, [1] site, [2] block
+constexpr int kWsNTiles = 4;   // number of query tiles in the list
+constexpr int kWsHeader = 8;   // ints; tile offsets follow, then the int4 list (16-B aligned)
+
+struct QTile {   // one query tile
+  int start;     // first token of the sequence (absolute row)
+  int q0;        // first query row of the tile, relative to `start`
+  int kv_lo;     // first key tile (relative to `start`, in kTileN units)
+  int len;       // sequence length
+};
+
+__device__ __forceinline__ int qtile_kv_lo(int q0, int window) {
+  if (window <= 0) return 0;
+  int lo = q0 - window + 1;
+  return lo > 0 ? lo / kTileN : 0;
+}
+
+__global__ void __launch_bounds__(kSchedThreads, 1)
+    schedule_kernel(const int32_t* __restrict__ cu, int num_seqs, int total_tokens, int window,
+                    int* __restrict__ ws, int* __restrict__ tile_off, int4* __restrict__ list,
+                    int max_tiles) {
+  __shared__ int s_scan[kSchedThreads];
+  __shared__ int s_hist[kCostBins];
+  __shared__ int s_cursor[kCostBins];
+  __shared__ int s_bad, s_base;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_bad = (cu[0] != 0 || cu[num_seqs] != total_tokens) ? 1 : 0;
+    s_base = 0;
+  }
+  for (int i = tid; i < kCostBins; i += kSchedThreads) {
+    s_hist[i] = 0;
+    s_cursor[i] = 0;
+  }
+  __syncthreads();
+
+  // Pass A: per-sequence tile counts -> exclusive prefix over sequences.
+  for (int c0 = 0; c0 < num_seqs; c0 += kSchedThreads) {
+    int s = c0 + tid;
+    int nt = 0;
+    if (s < num_seqs) {
+      int L = cu[s + 1] - cu[s];
+      if (L < 0) {
+        s_bad = 1;
+        L = 0;
+      }
+      nt = (L + kTileM - 1) / kTileM;
+    }
+    s_scan[tid] = nt;
+    __syncthreads();
+    for (int off = 1; off < kSchedThreads; off <<= 1) {  // Hillis-Steele inclusive scan
+      int v = tid >= off ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += v;
+      __syncthreads();
+    }
+    if (s < num_seqs) tile_off[s] = s_base + s_scan[tid] - nt;
+    __syncthreads();
+    if (tid == kSchedThreads - 1) s_base += s_scan[tid];
+    __syncthreads();
+  }
+  const int n_tiles = s_base;
+  if (tid == 0) tile_off[num_seqs] = n_tiles;
+  if (s_bad || n_tiles > max_tiles) {
+    if (tid == 0) {
+      ws[kWsNTiles] = 0;
+      if (atomicCAS(&ws[kWsStatus], 0, -8) == 0) ws[kWsStatus + 1] = 1000;
+    }
+    return;
+  }
+  __syncthreads();
+
+  // Pass B: cost histogram.  Tile i belongs to the last sequence whose offset <= i.
+  auto seq_of = [&](int i) {
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (tile_off[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  };
+  for (int i = tid; i < n_tiles; i += kSchedThreads) {
+    int s = seq_of(i);
+    int qt = i - tile_off[s];
+    int cost = qt - qtile_kv_lo(qt * kTileM, window) + 1;
+    atomicAdd(&s_hist[min(cost, kCostBins) - 1], 1);
+  }
+  __syncthreads();
+  // Exclusive offsets in descending cost order: bin b starts after all bins > b.
+  {
+    constexpr int per = kCostBins / kSchedThreads;
+    int local[per];
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      local[k] = s_hist[kCostBins - 1 - (tid * per + k)];
+      sum += local[k];
+    }
+    s_scan[tid] = sum;
+    __syncthreads();
+    for (int off = 1; off < kSchedThreads; off <<= 1) {
+      int v = tid >= off ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += v;
+      __syncthreads();
+    }
+    int run = s_scan[tid] - sum;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      s_cursor[kCostBins - 1 - (tid * per + k)] = run;
+      run += local[k];
+    }
+  }
+  __syncthreads();
+  // Pass C: scatter.
+  for (int i = tid; i < n_tiles; i += kSchedThreads) {
+    int s = seq_of(i);
+    int qt = i - tile_off[s];
+    int q0 = qt * kTileM;
+    int kv_lo = qtile_kv_lo(q0, window);
+    int cost = qt - kv_lo + 1;
+    int pos = atomicAdd(&s_cursor[min(cost, kCostBins) - 1], 1);
+    list[pos] = make_int4(cu[s], q0, kv_lo, cu[s + 1] - cu[s]);
+  }
+  if (tid == 0) ws[kWsNTiles] = n_tiles;
+}
+
+}  // namespace tsk

@@ -1,0 +1,322 @@
+// Host side of the C ABI declared in include/tsk_mha.h: argument checks,
+// TMA tensor-map encoding, the per-(device, stream) workspace, and the two
+// launches (scheduler pre-pass, persistent attention kernel).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "tsk_mha.h"
+#include "attention.cuh"
+#include "schedule.cuh"
+
+namespace {
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+
+struct Workspace {
+  int* base = nullptr;   // header ints, tile offsets, tile list
+  size_t bytes = 0;
+  int max_tiles = 0;
+  int max_seqs = 0;
+};
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  int num_sms = 0;
+  bool smem_set = false;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+std::map<int, DeviceState> g_dev;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool g_profile = false;
+cudaEvent_t g_ev[3] = {nullptr, nullptr, nullptr};
+int g_ev_dev = -1;
+bool g_ev_recorded = false;
+
+unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits give up after 2 s
+
+tsk_status cuda_fail(cudaError_t e) {
+  (void)cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? TSK_ERR_OOM : TSK_ERR_DEVICE;
+}
+
+tsk_status get_encoder() {
+  if (g_encode) return TSK_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return TSK_ERR_DEVICE;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return TSK_OK;
+}
+
+// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token); box = 64 x 1 x 128
+// rows of 128 bytes, stored with the 128-byte swizzle.
+tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H) {
+  cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {64 * 2, (cuuint64_t)H * 64 * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TSK_OK : TSK_ERR_DEVICE;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+tsk_status check_device(int* dev_out, DeviceState** st_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaErrorNoDevice);
+  DeviceState& st = g_dev[dev];
+  if (!st.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cuda_fail(cudaErrorInvalidDevice);
+    st.supported = (major == 10 && minor == 3);
+    st.checked = true;
+  }
+  if (!st.supported) return TSK_ERR_DEVICE;
+  if (!st.smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(tsk::attention_fwd_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tsk::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st.smem_set = true;
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return TSK_OK;
+}
+
+tsk_status get_workspace(int dev, cudaStream_t stream, int max_tiles, int num_seqs,
+                         Workspace** out) {
+  Workspace& w = g_ws[{dev, stream}];
+  if (w.base && w.max_tiles >= max_tiles && w.max_seqs >= num_seqs) {
+    *out = &w;
+    return TSK_OK;
+  }
+  int mt = max_tiles > w.max_tiles ? max_tiles : w.max_tiles;
+  int ms = num_seqs > w.max_seqs ? num_seqs : w.max_seqs;
+  mt = mt < 1024 ? 1024 : mt;
+  ms = ms < 1024 ? 1024 : ms;
+  size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ms + 1 + 3) & ~(size_t)3;
+  size_t bytes = off_ints * 4 + (size_t)mt * 16;
+  int* nb = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemsetAsync(nb, 0, bytes, stream);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(nb, stream);
+    return cuda_fail(e);
+  }
+  if (w.base) {
+    // Carry a pending device error over to the new buffer, then retire the old one.
+    cudaMemcpyAsync(nb, w.base, tsk::kWsHeader * 4, cudaMemcpyDeviceToDevice, stream);
+    cudaFreeAsync(w.base, stream);
+  }
+  w.base = nb;
+  w.bytes = bytes;
+  w.max_tiles = mt;
+  w.max_seqs = ms;
+  *out = &w;
+  return TSK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tsk_status_string(tsk_status s) {
+  switch (s) {
+    case TSK_OK: return "ok";
+    case TSK_ERR_INVALID_ARG: return "invalid argument";
+    case TSK_ERR_UNSUPPORTED: return "unsupported shape or size";
+    case TSK_ERR_ALIGNMENT: return "misaligned pointer";
+    case TSK_ERR_DEVICE: return "device error or unsupported device (needs compute capability 10.3)";
+    case TSK_ERR_OOM: return "out of device memory";
+    case TSK_ERR_LAUNCH: return "kernel launch failed";
+    case TSK_ERR_DEVICE_TIMEOUT: return "device-side bounded wait expired";
+    case TSK_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with total_tokens";
+  }
+  return "unknown status";
+}
+
+int32_t tsk_version(void) { return kVersion; }
+
+int32_t tsk_kernels_per_call(void) { return 2; }
+
+tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                           const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                           int32_t Hq, int32_t Hkv, int32_t D, int32_t window, float scale,
+                           void* out, float* lse, tsk_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // ---- host-only checks (no CUDA call before these pass)
+  if (!q || !k || !v || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
+  if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
+    return TSK_ERR_UNSUPPORTED;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
+  if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return TSK_ERR_ALIGNMENT;
+  if (!a4(cu_seqlens) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
+  const size_t qo_bytes = (size_t)total_tokens * Hq * D * 2;
+  const size_t kv_bytes = (size_t)total_tokens * Hkv * D * 2;
+  if (total_tokens > 0 && (overlaps(out, qo_bytes, q, qo_bytes) ||
+                           overlaps(out, qo_bytes, k, kv_bytes) ||
+                           overlaps(out, qo_bytes, v, kv_bytes)))
+    return TSK_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  DeviceState* ds = nullptr;
+  tsk_status st = check_device(&dev, &ds);
+  if (st != TSK_OK) return st;
+  if ((st = get_encoder()) != TSK_OK) return st;
+
+  const int64_t max_tiles64 = total_tokens / tsk::kTileM + num_seqs + 1;
+  const int max_tiles = (int)max_tiles64;
+  Workspace* ws = nullptr;
+  if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  if ((st = encode_thd(&tq, q, total_tokens, Hq)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, total_tokens, Hkv)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, total_tokens, Hkv)) != TSK_OK) return st;
+
+  char name[96];
+  snprintf(name, sizeof name, "tsk_mha_prefill[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,T=%lld]", Hq, Hkv,
+           D, window, num_seqs, (long long)total_tokens);
+  nvtxRangePushA(name);
+
+  const size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ws->max_seqs + 1 + 3) & ~(size_t)3;
+  int* tile_off = ws->base + tsk::kWsHeader;
+  int4* list = reinterpret_cast<int4*>(ws->base + off_ints);
+
+  const bool prof = g_profile;
+  if (prof) {
+    if (g_ev_dev != dev) {
+      for (auto& e : g_ev) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
+      }
+      for (auto& e : g_ev)
+        if (cudaEventCreate(&e) != cudaSuccess) {
+          nvtxRangePop();
+          return TSK_ERR_DEVICE;
+        }
+      g_ev_dev = dev;
+    }
+    cudaEventRecord(g_ev[0], stream);
+  }
+  tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
+      cu_seqlens, num_seqs, (int)total_tokens, window, ws->base, tile_off, list, ws->max_tiles);
+  if (prof) cudaEventRecord(g_ev[1], stream);
+
+  tsk::AttnParams p;
+  p.sinks = sinks;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.list = list;
+  p.ws = ws->base;
+  p.status = ws->base + tsk::kWsStatus;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.HP = (p.G + 1) / 2;
+  p.window = window;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  const int64_t units_bound = max_tiles64 * Hkv * p.HP;
+  const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
+  tsk::attention_fwd_kernel<<<grid, tsk::kThreads, tsk::kSmemBytes, stream>>>(tq, tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (prof) {
+    cudaEventRecord(g_ev[2], stream);
+    g_ev_recorded = true;
+  }
+  nvtxRangePop();
+  return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
+}
+
+tsk_status tsk_get_device_status(tsk_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TSK_ERR_DEVICE;
+  auto it = g_ws.find({dev, stream});
+  if (it == g_ws.end() || !it->second.base) return TSK_OK;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+  int hdr[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(hdr, it->second.base, sizeof hdr, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return cuda_fail(cudaErrorUnknown);
+  if (hdr[0] != 0) {
+    int zero[4] = {0, 0, 0, 0};
+    cudaMemcpy(it->second.base, zero, sizeof zero, cudaMemcpyHostToDevice);
+  }
+  return (tsk_status)hdr[0];
+}
+
+tsk_status tsk_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profile = enable != 0;
+  return TSK_OK;
+}
+
+tsk_status tsk_profile_read(float* prepass_ms, float* attention_ms) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ev_recorded) return TSK_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(g_ev[2]) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+  float a = 0.f, b = 0.f;
+  if (cudaEventElapsedTime(&a, g_ev[0], g_ev[1]) != cudaSuccess ||
+      cudaEventElapsedTime(&b, g_ev[1], g_ev[2]) != cudaSuccess)
+    return cuda_fail(cudaErrorUnknown);
+  if (prepass_ms) *prepass_ms = a;
+  if (attention_ms) *attention_ms = b;
+  return TSK_OK;
+}
+
+tsk_status tsk_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  if (!g_ws.empty() && cudaGetDevice(&dev) == cudaSuccess) cudaDeviceSynchronize();
+  for (auto& kv : g_ws)
+    if (kv.second.base) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.base);
+    }
+  if (dev >= 0) cudaSetDevice(dev);
+  g_ws.clear();
+  return TSK_OK;
+}
+
+// Test hook: shortens the device-side bounded waits (nanoseconds; 0 restores 2 s).
+tsk_status tsk_debug_set_wait_timeout_ns(unsigned long long ns) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_timeout_ns = ns ? ns : 2000000000ull;
+  return TSK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+/*
+ * tsk_mha.h -- C ABI of the GB300 (sm_103a) mha_prefill library.
+ *
+ * Operation (TokenSpeed-kernel README, section "Public API": `mha_prefill`;
+ * the workload is GPT-OSS attention -- grouped-query heads, attention sinks,
+ * sliding-window and full-attention layers -- page "TokenSpeed-kernel:
+ * multi-silicon ...", section "Числа: Gluon на AMD MI355X", and the ai-radar.it
+ * article, section "AMD MI355X: la prova sul campo").  The pages do not spell
+ * the formula out; this library computes, for every packed sequence s with
+ * tokens [start, start+L), token t, query head h and KV head g = h / (Hq/Hkv):
+ *
+ *     J   = { j : max(start, t - W + 1) <= j <= t }      (W <= 0: no lower window bound)
+ *     x_j = scale * <q[t,h,:], k[j,g,:]>
+ *     out[t,h,:] = sum_{j in J} e^{x_j} v[j,g,:] / (sum_{j in J} e^{x_j} + e^{sink_h})
+ *     lse[t,h]   = log(sum_{j in J} e^{x_j} + e^{sink_h})          (natural log)
+ *
+ * The sink is a raw logit (not multiplied by `scale`) that joins the softmax
+ * normaliser with a zero value vector; without sinks its term is absent.
+ *
+ * All entry points are host functions; pointers marked "device" must be
+ * device-accessible memory of the current CUDA device.  The caller owns every
+ * buffer; nothing is retained after a call returns.
+ */
+#ifndef TSK_MHA_H_
+#define TSK_MHA_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TSK_API __attribute__((visibility("default")))
+#else
+#define TSK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tsk_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  TSK_OK = 0,
+  TSK_ERR_INVALID_ARG = -1,    /* NULL where a buffer is required, negative sizes, bad scale */
+  TSK_ERR_UNSUPPORTED = -2,    /* D != 64, Hq % Hkv != 0, sizes beyond the limits below */
+  TSK_ERR_ALIGNMENT = -3,      /* q/k/v/out not 16-byte aligned, sinks/lse/cu not 4-byte */
+  TSK_ERR_DEVICE = -4,         /* no device, not compute capability 10.3, CUDA error */
+  TSK_ERR_OOM = -5,            /* workspace allocation failed */
+  TSK_ERR_LAUNCH = -6,         /* kernel launch failed */
+  TSK_ERR_DEVICE_TIMEOUT = -7, /* a kernel gave up on a bounded wait (device status word) */
+  TSK_ERR_BAD_SEQLENS = -8     /* device check: cu_seqlens not 0..total_tokens non-decreasing */
+} tsk_status;
+
+/*
+ * tsk_mha_prefill -- causal grouped-query attention with sink and window
+ * over packed variable-length sequences (the formula above).
+ *
+ *   q           device, bf16 [total_tokens, Hq, D], contiguous (row stride Hq*D)
+ *   k, v        device, bf16 [total_tokens, Hkv, D], contiguous
+ *   sinks       device, fp32 [Hq] sink logits, or NULL for no sink
+ *   cu_seqlens  device, int32 [num_seqs + 1]; cu[0] = 0, non-decreasing,
+ *               cu[num_seqs] = total_tokens.  Zero-length sequences are allowed.
+ *   num_seqs    number of packed sequences (>= 0)
+ *   total_tokens host copy of cu_seqlens[num_seqs] (the tensor-map extent; the
+ *               kernels check it against the device array and report
+ *               TSK_ERR_BAD_SEQLENS through tsk_get_device_status on mismatch,
+ *               computing nothing in that case)
+ *   Hq, Hkv     query / KV heads; Hq % Hkv == 0 (Hq == Hkv is plain MHA)
+ *   D           head dimension; must be 64
+ *   window      <= 0: full causal; W >= 1: token t sees keys t-W+1 .. t
+ *   scale       multiplier of q.k (finite, > 0); not applied to sinks
+ *   out         device, bf16 [total_tokens, Hq, D]; must not overlap q, k, v
+ *   lse         device, fp32 [total_tokens, Hq] natural-log normaliser, or NULL
+ *   stream      stream to enqueue on
+ *
+ * Limits: total_tokens * Hq < 2^31, num_seqs < 2^24.
+ * Asynchronous: enqueues work on `stream` and returns; no host synchronisation.
+ * Results are bitwise deterministic run to run (no split-K, no atomics in the
+ * arithmetic).  Host-detectable errors return before anything is enqueued and
+ * leave all memory untouched.  The library keeps a small device workspace per
+ * (device, stream), created on first use; calls on one stream are ordered,
+ * calls on different streams do not share it.  Not safe to call concurrently
+ * from several host threads on the same stream.
+ */
+TSK_API tsk_status tsk_mha_prefill(const void *q, const void *k, const void *v, const float *sinks,
+                           const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                           int32_t Hq, int32_t Hkv, int32_t D, int32_t window, float scale,
+                           void *out, float *lse, tsk_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+TSK_API const char *tsk_status_string(tsk_status s);
+
+/*
+ * Synchronises `stream`, reads and clears the device status word of that
+ * stream's workspace: TSK_OK, TSK_ERR_DEVICE_TIMEOUT (a bounded wait expired;
+ * that call's outputs are incomplete) or TSK_ERR_BAD_SEQLENS.  Returns TSK_OK
+ * if the stream has no workspace yet.
+ */
+TSK_API tsk_status tsk_get_device_status(tsk_stream_t stream);
+
+/*
+ * Timing hook.  While enabled, each tsk_mha_prefill call records CUDA events
+ * on its stream around the scheduler pre-pass and around the attention
+ * kernel.  tsk_profile_read synchronises on the last call's events and returns
+ * the two durations in milliseconds.
+ */
+TSK_API tsk_status tsk_profile_enable(int enable);
+TSK_API tsk_status tsk_profile_read(float *prepass_ms, float *attention_ms);
+
+/* Number of kernels one tsk_mha_prefill call launches (0 for empty problems). */
+TSK_API int32_t tsk_kernels_per_call(void);
+
+/* Frees every cached workspace (synchronises the device first). */
+TSK_API tsk_status tsk_release(void);
+
+/*
+ * Test hook: sets the limit of every device-side bounded wait of later calls
+ * (nanoseconds; 0 restores the default of 2 s).  With a tiny limit the
+ * attention kernel gives up early, records TSK_ERR_DEVICE_TIMEOUT, drains its
+ * in-flight copies and MMAs (those keep a 2 s limit), frees TMEM and returns,
+ * leaving the outputs incomplete; the CUDA context stays usable.
+ */
+TSK_API tsk_status tsk_debug_set_wait_timeout_ns(unsigned long long ns);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+TSK_API int32_t tsk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSK_MHA_H_ */

@@ -1,0 +1,82 @@
+"""Shared helpers for GPU parity tests: run the CUDA path through the C ABI on
+a seeded workload and compare with the CPU oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+import inputgen
+import oracle
+
+# Tolerances for bf16 I/O: outputs max |d| <= 2e-2 and mean |d| <= 2e-3;
+# LSE |d| <= 1e-3 absolute.
+OUT_MAX = 2e-2
+OUT_MEAN = 2e-3
+LSE_MAX = 1e-3
+
+
+def to_device(w: inputgen.Workload, device="cuda"):
+    import torch
+    d = {
+        "q": torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device),
+        "k": torch.from_numpy(w.k.view(np.int16)).view(torch.bfloat16).to(device),
+        "v": torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).to(device),
+        "cu": torch.from_numpy(w.cu_seqlens).to(device),
+        "sinks": None if w.sinks is None else torch.from_numpy(w.sinks).to(device),
+    }
+    return d
+
+
+def run_gpu(w: inputgen.Workload, d=None, with_lse=True, check_status=True):
+    """Returns (out bf16 torch [T,Hq,D], lse fp32 torch [T,Hq] or None)."""
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    d = d or to_device(w)
+    T = w.total_tokens
+    out = torch.full((T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=d["q"].device)
+    lse = torch.full((T, w.Hq), float("nan"), dtype=torch.float32, device=d["q"].device) \
+        if with_lse else None
+    rc = pkg.tsk_mha_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu"], w.num_seqs, T, w.Hq,
+                             w.Hkv, w.D, w.window, w.scale, out, lse)
+    assert rc == 0, pkg.STATUS.get(rc, rc)
+    torch.cuda.synchronize()
+    if check_status:
+        st = pkg.tsk_get_device_status()
+        assert st == 0, pkg.STATUS.get(st, st)
+    return out, lse
+
+
+def compare(gpu_out, gpu_lse, ref_out, ref_lse, label=""):
+    """gpu_*: numpy float64 (any shape matching ref_*)."""
+    assert np.isfinite(gpu_out).all(), f"{label}: non-finite outputs"
+    d = np.abs(gpu_out - ref_out)
+    msg = f"{label}: out max {d.max():.3g} mean {d.mean():.3g}"
+    assert d.max() <= OUT_MAX and d.mean() <= OUT_MEAN, msg
+    if gpu_lse is not None:
+        assert np.isfinite(gpu_lse).all(), f"{label}: non-finite lse"
+        dl = np.abs(gpu_lse - ref_lse)
+        msg += f", lse max {dl.max():.3g}"
+        assert dl.max() <= LSE_MAX, msg
+    return msg
+
+
+def check_full(w: inputgen.Workload, with_lse=True, label=None):
+    out, lse = run_gpu(w, with_lse=with_lse)
+    ro, rl, _ = oracle.run_workload(w)
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64) if with_lse else None
+    return compare(o, l, ro, rl, label or w.name)
+
+
+def check_sampled(w: inputgen.Workload, n_rows=4096, label=None, d=None):
+    out, lse = run_gpu(w, d=d)
+    t, h = inputgen.sample_rows(w, n_target=n_rows)
+    assert len(t) >= min(n_rows, w.total_tokens * w.Hq)
+    ro, rl, _ = oracle.run_workload(w, rows=(t, h))
+    import torch
+    ti = torch.from_numpy(t).to(out.device)
+    hi = torch.from_numpy(h.astype(np.int64)).to(out.device)
+    o = out[ti, hi].float().cpu().numpy().astype(np.float64)
+    l = lse[ti, hi].cpu().numpy().astype(np.float64)
+    # every output must be finite, not only the sampled rows
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all()), "non-finite rows"
+    return compare(o, l, ro, rl, (label or w.name) + f" [{len(t)} rows]")

@@ -1,0 +1,140 @@
+"""CUDA path (through the C ABI) against the CPU oracle on seeded inputs."""
+import numpy as np
+import pytest
+
+import inputgen
+import oracle
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import gqa_attention_prefill_gb300 as pkg
+    from gqa_attention_prefill_gb300 import build
+    build.build()
+    pkg.load_library()
+
+
+# ------------------------------------------------------------------ full checks (every row)
+def test_tiny_config_full():
+    print(parity.check_full(inputgen.config("tiny_1x256_h4kv1")))
+
+
+@pytest.mark.parametrize("seqlens", [[1], [2], [127], [128], [129], [255], [257],
+                                     [1, 2, 127, 128, 129, 255, 257], [0, 300, 0, 5, 0]])
+def test_edge_lengths(seqlens):
+    w = inputgen.make(seqlens, 8, 2, seed=sum(seqlens) + len(seqlens))
+    print(parity.check_full(w, label=f"L={seqlens}"))
+
+
+@pytest.mark.parametrize("window", [1, 2, 127, 128, 129, 200, 1000])
+def test_windows(window):
+    w = inputgen.make([1, 127, 128, 129, 300, 640], 8, 2, window=window, seed=window)
+    print(parity.check_full(w, label=f"W={window}"))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 1), (6, 2), (3, 1), (16, 2), (64, 8)])
+def test_head_groupings(Hq, Hkv):
+    w = inputgen.make([200, 333], Hq, Hkv, seed=Hq * 10 + Hkv)
+    print(parity.check_full(w, label=f"Hq={Hq},Hkv={Hkv}"))
+
+
+def test_no_sinks_and_no_lse():
+    w = inputgen.make([130, 257], 8, 2, window=0, seed=4, with_sinks=False)
+    print(parity.check_full(w, label="no sinks"))
+    print(parity.check_full(w, with_lse=False, label="no sinks, no lse"))
+    w = inputgen.make([130, 257], 8, 2, window=64, seed=5, with_sinks=False)
+    print(parity.check_full(w, label="no sinks, W=64"))
+
+
+def test_extreme_sinks_and_scales():
+    w = inputgen.make([300], 8, 2, seed=6, sink_sigma=6.0, scale=0.3)
+    print(parity.check_full(w, label="sinks N(0,6), scale 0.3"))
+    w = inputgen.make([700], 8, 2, seed=7, k_mult=4.0, scale=0.125)
+    print(parity.check_full(w, label="peaky K x4"))
+
+
+def test_window_config_full():
+    print(parity.check_full(inputgen.config("window128_4x4096_h64kv8")))
+
+
+# ------------------------------------------------------------------ full-size sampled
+@pytest.mark.parametrize("name", ["causal_4x4096_h64kv8", "ragged32_h64kv8",
+                                  "ragged32_w128_h64kv8", "long_1x32768_h64kv8"])
+def test_large_configs_sampled(name):
+    print(parity.check_sampled(inputgen.config(name)))
+
+
+# ------------------------------------------------------------------ properties
+def test_deterministic_bitwise():
+    import torch
+    w = inputgen.make([1000, 3000], 16, 2, seed=9)
+    d = parity.to_device(w)
+    o1, l1 = parity.run_gpu(w, d)
+    o2, l2 = parity.run_gpu(w, d)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def test_streams_and_repeat_calls():
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    w = inputgen.make([500, 77], 8, 2, seed=10)
+    d = parity.to_device(w)
+    ref, _ = parity.run_gpu(w, d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse = pkg.mha_prefill(d["q"], d["k"], d["v"], d["cu"], sinks=d["sinks"],
+                                   window=w.window, scale=w.scale)
+    s.synchronize()
+    assert pkg.tsk_get_device_status(s) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_bad_seqlens_reported_on_device():
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    w = inputgen.make([100, 50], 4, 1, seed=11)
+    d = parity.to_device(w)
+    out = torch.zeros((150, 4, 64), dtype=torch.bfloat16, device="cuda")
+    # total_tokens disagrees with cu_seqlens[-1]
+    rc = pkg.tsk_mha_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu"], 2, 149, 4, 1, 64, 0,
+                             0.125, out, None)
+    assert rc == 0
+    assert pkg.tsk_get_device_status() == -8
+    assert bool((out == 0).all())           # nothing computed
+    bad = torch.tensor([0, 120, 100, 150], dtype=torch.int32, device="cuda")
+    rc = pkg.tsk_mha_prefill(d["q"], d["k"], d["v"], d["sinks"], bad, 3, 150, 4, 1, 64, 0,
+                             0.125, out, None)
+    assert rc == 0 and pkg.tsk_get_device_status() == -8
+    assert pkg.tsk_get_device_status() == 0  # cleared by the read
+    print(parity.check_full(w, label="after bad calls"))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    import gqa_attention_prefill_gb300 as pkg
+    w = inputgen.make([4096] * 2, 16, 2, seed=12)
+    d = parity.to_device(w)
+    pkg.tsk_debug_set_wait_timeout_ns(1)   # every wait that does not succeed at once gives up
+    try:
+        out, lse = parity.run_gpu(w, d, check_status=False)
+        st = pkg.tsk_get_device_status()
+    finally:
+        pkg.tsk_debug_set_wait_timeout_ns(0)
+    assert st == -7
+    print(parity.check_full(w, label="after timeout"))   # context usable, results right again
+
+
+def test_python_wrapper_validation():
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    q = torch.zeros((10, 4, 64), dtype=torch.float16, device="cuda")
+    k = torch.zeros((10, 1, 64), dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 10], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        pkg.mha_prefill(q, k, k, cu)
+    q = q.to(torch.bfloat16)
+    with pytest.raises(pkg.TskError):
+        pkg.mha_prefill(q, k, k, cu, scale=-1.0)
