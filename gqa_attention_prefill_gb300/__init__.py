@@ -40,7 +40,10 @@ class TskError(RuntimeError):
 
 
 def library_path() -> str:
-    return _LIB_PATH
+    """The library file to load: $TSK_LIB_PATH if set (another build of the
+    same sources, e.g. with different compile-time options), else the in-tree
+    libtsk_mha.so."""
+    return os.environ.get("TSK_LIB_PATH") or _LIB_PATH
 
 
 def load_library():
@@ -49,10 +52,11 @@ def load_library():
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(_LIB_PATH):
-            raise RuntimeError(f"{_LIB_PATH} is missing: run __graft_entry__.build() "
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: run __graft_entry__.build() "
                                "(or python -m gqa_attention_prefill_gb300.build)")
-        lib = ctypes.CDLL(_LIB_PATH)
+        lib = ctypes.CDLL(path)
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         lib.tsk_mha_prefill.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32,
                                         ctypes.c_float, P, P, P]
@@ -70,8 +74,8 @@ def load_library():
         lib.tsk_kernels_per_call.restype = i32
         lib.tsk_release.argtypes = []
         lib.tsk_release.restype = ctypes.c_int
-        lib.tsk_debug_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
-        lib.tsk_debug_set_wait_timeout_ns.restype = ctypes.c_int
+        lib.tsk_debug_set_wait.argtypes = [ctypes.c_ulonglong, ctypes.c_int]
+        lib.tsk_debug_set_wait.restype = ctypes.c_int
         lib.tsk_version.argtypes = []
         lib.tsk_version.restype = i32
         _lib = lib
@@ -165,8 +169,9 @@ def tsk_profile_read():
     return a.value, b.value
 
 
-def tsk_debug_set_wait_timeout_ns(ns: int) -> int:
-    return load_library().tsk_debug_set_wait_timeout_ns(int(ns))
+def tsk_debug_set_wait(timeout_ns: int = 0, stall: bool = False) -> int:
+    """Test hook: device wait limit for later calls (0 = 2 s) and stall injection."""
+    return load_library().tsk_debug_set_wait(int(timeout_ns), 1 if stall else 0)
 
 
 def tsk_kernels_per_call() -> int:

@@ -37,20 +37,30 @@ def stale() -> bool:
     return any(os.path.getmtime(d) > t for d in DEPS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not stale():
+def build(force: bool = False, verbose: bool = False, out: str | None = None,
+          defines=()) -> str:
+    """Builds libtsk_mha.so (or `out`, with extra -D `defines`, always rebuilt)."""
+    target = out or LIB
+    if out is None and not defines and not force and not stale():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *flags(verbose), "-o", tmp, *SOURCES]
+    tmp = target + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *flags(verbose), *[f"-D{d}" for d in defines], "-o", tmp, *SOURCES]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc failed building libtsk_mha.so")
     if verbose:
         sys.stderr.write(r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    import argparse
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("-v", action="store_true")
+    ap.add_argument("--out")
+    ap.add_argument("-D", action="append", default=[])
+    a = ap.parse_args()
+    print(build(force=a.force, verbose=a.v, out=a.out, defines=a.D))

@@ -36,7 +36,14 @@
 
 namespace tsk {
 
-constexpr int kStages = 3;
+#ifndef TSK_KV_STAGES
+#define TSK_KV_STAGES 3
+#endif
+#ifndef TSK_RESCALE_THRESHOLD
+#define TSK_RESCALE_THRESHOLD 8.0f
+#endif
+constexpr int kStages = TSK_KV_STAGES;           // K/V ring depth
+constexpr float kRescaleThreshold = TSK_RESCALE_THRESHOLD;  // log2 units
 constexpr int kThreads = 384;
 constexpr int kHeadDim = 64;
 constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // 16 KB (also K/V tiles)
@@ -63,6 +70,7 @@ struct AttnParams {
   int window;
   float scale_log2;     // scale * log2(e)
   unsigned long long timeout_ns;
+  int debug_stall;      // test hook: producer first waits on a barrier nothing signals
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.
@@ -77,7 +85,8 @@ enum : int {
   kBarPFull = 8 + 3 * kStages,  // [2]
   kBarPVDone = 10 + 3 * kStages,  // [2]
   kBarDrain = 12 + 3 * kStages,
-  kNumBars = 13 + 3 * kStages
+  kBarNever = 13 + 3 * kStages,  // never signalled (stall injection)
+  kNumBars = 14 + 3 * kStages
 };
 
 // mbar_wait for warps whose every lane polls: the result is made warp-uniform
@@ -110,16 +119,318 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   return r;
 }
 
+// State shared by the roles of one CTA.
+struct Ctx {
+  uint32_t sbase;   // 1 KB-aligned shared memory base (shared-window address)
+  uint32_t bar0;    // first mbarrier
+  uint32_t tmem;    // TMEM base address
+  int total_units;
+  WaitCtl wc;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ WaitCtl drain_ctl(const WaitCtl& wc, int* dummy_abort) {
+  WaitCtl dc = wc;
+  dc.abort_flag = dummy_abort;
+  if (dc.timeout_ns < kDrainTimeoutNs) dc.timeout_ns = kDrainTimeoutNs;
+  return dc;
+}
+
+// TMA producer (one thread).
+__device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* tmQ,
+                                           const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                           const AttnParams& p) {
+  // ------------------------------------------------------------ producer
+  uint32_t q_iter = 0, kv_iter = 0;
+  bool ok = true;
+  if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, cx.wc, 99);
+  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    const int qb = q_iter & 1;
+    if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, cx.wc, 1);
+    if (!ok) break;
+    mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), w.ntiles * kTileBytes);
+    for (int t = 0; t < w.ntiles; ++t)
+      tma_load_3d(cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes, tmQ, cx.bar(kBarQFull + qb), 0,
+                  w.h0 + t, w.start + w.q0);
+    ++q_iter;
+    for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
+      const int s = kv_iter % kStages;
+      const uint32_t k = kv_iter / kStages;
+      if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, cx.wc, 2);
+      if (!ok) break;
+      const int row = w.start + (w.kv_lo + j) * kTileN;
+      const uint32_t kdst = cx.sbase + kSmemKV + s * 2 * kTileBytes;
+      mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTileBytes);
+      tma_load_3d(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, row);
+      mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kTileBytes);
+      tma_load_3d(kdst + kTileBytes, tmV, cx.bar(kBarVFull + s), 0, w.g, row);
+    }
+  }
+  // Drain: wait for the last load issued into every buffer so that no
+  // copy is still in flight when the CTA exits (bounded, best effort).
+  int dummy_abort = 0;
+  const WaitCtl dc = drain_ctl(cx.wc, &dummy_abort);
+  for (uint32_t i = (kv_iter > kStages ? kv_iter - kStages : 0); i < kv_iter; ++i) {
+    mbar_wait(cx.bar(kBarKFull + i % kStages), (i / kStages) & 1, dc, 11);
+    mbar_wait(cx.bar(kBarVFull + i % kStages), (i / kStages) & 1, dc, 12);
+  }
+  for (uint32_t i = (q_iter > 2 ? q_iter - 2 : 0); i < q_iter; ++i)
+    mbar_wait(cx.bar(kBarQFull + (i & 1)), (i >> 1) & 1, dc, 13);
+
+}
+
+// tcgen05.mma issuer (one thread).
+__device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p) {
+  // ------------------------------------------------------------ MMA issuer
+  uint32_t q_iter = 0, kv_iter = 0;
+  uint32_t s_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
+  bool ok = true;
+  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    const int qb = q_iter & 1;
+    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, cx.wc, 3);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t qaddr = cx.sbase + kSmemQ + 2 * qb * kTileBytes;
+    auto issue_s = [&](int t, int stage) {
+      const uint32_t a = qaddr + t * kTileBytes;
+      const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        mma_ss(cx.tmem + kColS0 + 128 * t, sdesc_sw128(a + 32 * kk), sdesc_sw128(b + 32 * kk),
+               kIdescQK, kk > 0 ? 1u : 0u);
+      tc_commit(cx.bar(kBarSFull + t));
+    };
+    auto issue_pv = [&](int t, int stage, bool acc) {
+      const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes + kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_ts(cx.tmem + kColO0 + 64 * t, cx.tmem + kColP0 + 64 * t + 8 * kk,
+               sdesc_sw128(b + 2048 * kk), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      tc_commit(cx.bar(kBarPVDone + t));
+    };
+    // S_t(0)
+    {
+      const int s0 = kv_iter % kStages;
+      ok = mbar_wait(cx.bar(kBarKFull + s0), (kv_iter / kStages) & 1, cx.wc, 4);
+      if (!ok) break;
+      tc_fence_after();
+      for (int t = 0; t < w.ntiles && ok; ++t) {
+        if (s_cnt[t] > 0) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt[t] - 1) & 1, cx.wc, 5);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(t, s0);
+        ++s_cnt[t];
+      }
+    }
+    for (int j = 0; j < w.n_kv && ok; ++j) {
+      const uint32_t cur = kv_iter + j;
+      const int sc = cur % kStages;
+      const int sn = (cur + 1) % kStages;
+      if (j + 1 < w.n_kv) {
+        // S_t(j+1) for both tiles first, so neither softmax waits on the other's P.
+        ok = mbar_wait(cx.bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, cx.wc, 6);
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < w.ntiles; ++t) {
+          ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt[t] - 1) & 1, cx.wc, 5);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t, sn);
+          ++s_cnt[t];
+        }
+        if (!ok) break;
+      }
+      ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStages) & 1, cx.wc, 7);
+      if (!ok) break;
+      tc_fence_after();
+      for (int t = 0; t < w.ntiles; ++t) {
+        ok = mbar_wait(cx.bar(kBarPFull + t), p_cnt[t] & 1, cx.wc, 8);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(t, sc, j > 0);
+        ++p_cnt[t];
+      }
+      if (!ok) break;
+      tc_commit(cx.bar(kBarKVEmpty + sc));
+    }
+    if (!ok) break;
+    kv_iter += w.n_kv;
+    tc_commit(cx.bar(kBarQEmpty + qb));
+    ++q_iter;
+  }
+  // Make sure no MMA is still running before TMEM is freed.
+  tc_commit(cx.bar(kBarDrain));
+  int dummy_abort = 0;
+  const WaitCtl dc = drain_ctl(cx.wc, &dummy_abort);
+  mbar_wait(cx.bar(kBarDrain), 0, dc, 14);
+
+}
+
+// Softmax and epilogue of one query tile (one warpgroup, one thread per row).
+__device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p, int warp,
+                                          int lane) {
+  // -------------------------------------------------------------- softmax
+  const int t = (warp - 4) >> 2;    // query tile of this warpgroup
+  const int wq = warp & 3;          // TMEM lane quarter
+  const int r = wq * 32 + lane;     // query row within the tile
+  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  const uint32_t tS = cx.tmem + lane_base + kColS0 + 128 * t;
+  const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
+  const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
+  const float sl2 = p.scale_log2;
+  uint32_t s_cnt = 0, pv_cnt = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    if (t >= w.ntiles) continue;
+    const int h = w.h0 + t;
+    const int row = w.q0 + r;  // relative to sequence start
+    float m_used = -INFINITY, l = 0.f;
+    if (p.sinks) {
+      m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
+      l = 1.f;
+    }
+    for (int j = 0; j < w.n_kv; ++j) {
+      const int kt = w.kv_lo + j;
+      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, cx.wc, 9);
+      if (!ok) break;
+      ++s_cnt;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld_32x32b_x32(tS + 0, sr + 0);
+      tmem_ld_32x32b_x32(tS + 32, sr + 32);
+      tmem_ld_32x32b_x32(tS + 64, sr + 64);
+      tmem_ld_32x32b_x32(tS + 96, sr + 96);
+      tmem_wait_ld();
+      reg_fence<128>(sr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      const int kbase = kt * kTileN;
+      const bool edge = (kbase + kTileN - 1 > w.q0) ||
+                        (p.window > 0 && kbase < w.q0 + kTileM - p.window);
+      if (edge) {
+        const int hi_c = row - kbase;
+        const int lo_c = p.window > 0 ? row - p.window + 1 - kbase : -1;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > hi_c || c < lo_c) s[c] = -INFINITY;
+      }
+      // Row maximum: four independent chains of 3-input max.
+      float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 8) {
+        m0 = max3f(m0, s[c + 0], s[c + 1]);
+        m1 = max3f(m1, s[c + 2], s[c + 3]);
+        m2 = max3f(m2, s[c + 4], s[c + 5]);
+        m3 = max3f(m3, s[c + 6], s[c + 7]);
+      }
+      const float m_tile = max3f(m0, m1, fmaxf(m2, m3)) * sl2;
+      float alpha = 1.f;
+      const bool need = m_tile > m_used + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        if (m_tile > m_used) {
+          alpha = ex2_approx(m_used - m_tile);  // m_used = -inf gives 0
+          m_used = m_tile;
+        }
+      }
+      l *= alpha;
+      const float m_use = m_used == -INFINITY ? 0.f : m_used;
+      // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per
+      // element, four packed partial sums, bf16x2 packing for TMEM.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negm = f2_pack(-m_use, -m_use);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm), x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        const uint64_t pp = f2_pack(p0, p1);
+        acc[c & 3] = c < 4 ? pp : f2_add(acc[c & 3], pp);
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      {
+        const uint64_t a01 = f2_add(acc[0], acc[1]);
+        const uint64_t a23 = f2_add(acc[2], acc[3]);
+        float r0, r1;
+        f2_unpack(f2_add(a01, a23), r0, r1);
+        l += r0 + r1;
+      }
+      if (j > 0) {
+        // O_t is stable and P_t reusable once PV_t(j-1) has completed.
+        ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, cx.wc, 10);
+        if (!ok) break;
+        ++pv_cnt;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t o[64];
+          tmem_ld_32x32b_x32(tO, o);
+          tmem_ld_32x32b_x32(tO + 32, o + 32);
+          tmem_wait_ld();
+          reg_fence<64>(o);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st_32x32b_x32(tO, o);
+          tmem_st_32x32b_x32(tO + 32, o + 32);
+        }
+      }
+      tmem_st_32x32b_x32(tP, pk);
+      tmem_st_32x32b_x32(tP + 32, pk + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
+    }
+    if (!ok) break;
+    // ------------------------------------------------------------ epilogue
+    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, cx.wc, 10);
+    if (!ok) break;
+    ++pv_cnt;
+    tc_fence_after();
+    uint32_t o[64];
+    tmem_ld_32x32b_x32(tO, o);
+    tmem_ld_32x32b_x32(tO + 32, o + 32);
+    tmem_wait_ld();
+    reg_fence<64>(o);
+    if (row < w.len) {
+      const float inv = 1.f / l;
+      const size_t orow = (size_t)(w.start + row) * p.Hq + h;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+        v.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+        v.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+        v.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+        dst[c] = v;
+      }
+      if (p.lse) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    }
+    tc_fence_before();
+  }
+
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + kSmemBar;
-  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  Ctx cx;
+  cx.sbase = smem_u32(smem);
+  cx.bar0 = cx.sbase + kSmemBar;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemBar + 8 * kNumBars + 4);
 
@@ -128,19 +439,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarQFull + i), 1);
-      mbar_init(bar(kBarQEmpty + i), 1);
-      mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSFree + i), 4);
-      mbar_init(bar(kBarPFull + i), 4);
-      mbar_init(bar(kBarPVDone + i), 1);
+      mbar_init(cx.bar(kBarQFull + i), 1);
+      mbar_init(cx.bar(kBarQEmpty + i), 1);
+      mbar_init(cx.bar(kBarSFull + i), 1);
+      mbar_init(cx.bar(kBarSFree + i), 4);
+      mbar_init(cx.bar(kBarPFull + i), 4);
+      mbar_init(cx.bar(kBarPVDone + i), 1);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarKVEmpty + s), 1);
+      mbar_init(cx.bar(kBarKFull + s), 1);
+      mbar_init(cx.bar(kBarVFull + s), 1);
+      mbar_init(cx.bar(kBarKVEmpty + s), 1);
     }
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(cx.bar(kBarDrain), 1);
+    mbar_init(cx.bar(kBarNever), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -156,268 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  cx.tmem = *tmem_slot;
+  cx.wc = WaitCtl{abort_flag, p.status, p.timeout_ns};
+  cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
 
-  WaitCtl wc{abort_flag, p.status, p.timeout_ns};
-  const int n_qtiles = p.ws[kWsNTiles];
-  const int total_units = n_qtiles * p.Hkv * p.HP;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      uint32_t q_iter = 0, kv_iter = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
-        const int qb = q_iter & 1;
-        if (q_iter >= 2) ok = mbar_wait(bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, wc, 1);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(kBarQFull + qb), w.ntiles * kTileBytes);
-        for (int t = 0; t < w.ntiles; ++t)
-          tma_load_3d(sbase + kSmemQ + (2 * qb + t) * kTileBytes, &tmQ, bar(kBarQFull + qb), 0,
-                      w.h0 + t, w.start + w.q0);
-        ++q_iter;
-        for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
-          const int s = kv_iter % kStages;
-          const uint32_t k = kv_iter / kStages;
-          if (k >= 1) ok = mbar_wait(bar(kBarKVEmpty + s), (k - 1) & 1, wc, 2);
-          if (!ok) break;
-          const int row = w.start + (w.kv_lo + j) * kTileN;
-          const uint32_t kdst = sbase + kSmemKV + s * 2 * kTileBytes;
-          mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-          tma_load_3d(kdst, &tmK, bar(kBarKFull + s), 0, w.g, row);
-          mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-          tma_load_3d(kdst + kTileBytes, &tmV, bar(kBarVFull + s), 0, w.g, row);
-        }
-      }
-      // Drain: wait for the last load issued into every buffer so that no
-      // copy is still in flight when the CTA exits (bounded, best effort).
-      WaitCtl dc = wc;
-      int dummy_abort = 0;
-      dc.abort_flag = &dummy_abort;
-      if (dc.timeout_ns < kDrainTimeoutNs) dc.timeout_ns = kDrainTimeoutNs;
-      for (uint32_t i = (kv_iter > kStages ? kv_iter - kStages : 0); i < kv_iter; ++i) {
-        mbar_wait(bar(kBarKFull + i % kStages), (i / kStages) & 1, dc, 11);
-        mbar_wait(bar(kBarVFull + i % kStages), (i / kStages) & 1, dc, 12);
-      }
-      for (uint32_t i = (q_iter > 2 ? q_iter - 2 : 0); i < q_iter; ++i)
-        mbar_wait(bar(kBarQFull + (i & 1)), (i >> 1) & 1, dc, 13);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      uint32_t q_iter = 0, kv_iter = 0;
-      uint32_t s_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
-      bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
-        const int qb = q_iter & 1;
-        ok = mbar_wait(bar(kBarQFull + qb), (q_iter >> 1) & 1, wc, 3);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t qaddr = sbase + kSmemQ + 2 * qb * kTileBytes;
-        auto issue_s = [&](int t, int stage) {
-          const uint32_t a = qaddr + t * kTileBytes;
-          const uint32_t b = sbase + kSmemKV + stage * 2 * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            mma_ss(tmem + kColS0 + 128 * t, sdesc_sw128(a + 32 * kk), sdesc_sw128(b + 32 * kk),
-                   kIdescQK, kk > 0 ? 1u : 0u);
-          tc_commit(bar(kBarSFull + t));
-        };
-        auto issue_pv = [&](int t, int stage, bool acc) {
-          const uint32_t b = sbase + kSmemKV + stage * 2 * kTileBytes + kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ts(tmem + kColO0 + 64 * t, tmem + kColP0 + 64 * t + 8 * kk,
-                   sdesc_sw128(b + 2048 * kk), kIdescPV, (acc || kk > 0) ? 1u : 0u);
-          tc_commit(bar(kBarPVDone + t));
-        };
-        // S_t(0)
-        {
-          const int s0 = kv_iter % kStages;
-          ok = mbar_wait(bar(kBarKFull + s0), (kv_iter / kStages) & 1, wc, 4);
-          if (!ok) break;
-          tc_fence_after();
-          for (int t = 0; t < w.ntiles && ok; ++t) {
-            if (s_cnt[t] > 0) ok = mbar_wait(bar(kBarSFree + t), (s_cnt[t] - 1) & 1, wc, 5);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(t, s0);
-            ++s_cnt[t];
-          }
-        }
-        for (int j = 0; j < w.n_kv && ok; ++j) {
-          const uint32_t cur = kv_iter + j;
-          const int sc = cur % kStages;
-          const bool more = j + 1 < w.n_kv;
-          const int sn = (cur + 1) % kStages;
-          if (more) {
-            ok = mbar_wait(bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, wc, 6);
-            if (!ok) break;
-          }
-          ok = mbar_wait(bar(kBarVFull + sc), (cur / kStages) & 1, wc, 7);
-          if (!ok) break;
-          tc_fence_after();
-          for (int t = 0; t < w.ntiles; ++t) {
-            if (more) {
-              ok = mbar_wait(bar(kBarSFree + t), (s_cnt[t] - 1) & 1, wc, 5);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(t, sn);
-              ++s_cnt[t];
-            }
-            ok = mbar_wait(bar(kBarPFull + t), p_cnt[t] & 1, wc, 8);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, sc, j > 0);
-            ++p_cnt[t];
-          }
-          if (!ok) break;
-          tc_commit(bar(kBarKVEmpty + sc));
-        }
-        if (!ok) break;
-        kv_iter += w.n_kv;
-        tc_commit(bar(kBarQEmpty + qb));
-        ++q_iter;
-      }
-      // Make sure no MMA is still running before TMEM is freed.
-      tc_commit(bar(kBarDrain));
-      WaitCtl dc = wc;
-      int dummy_abort = 0;
-      dc.abort_flag = &dummy_abort;
-      if (dc.timeout_ns < kDrainTimeoutNs) dc.timeout_ns = kDrainTimeoutNs;
-      mbar_wait(bar(kBarDrain), 0, dc, 14);
-    }
-  } else if (warp >= 4) {
-    // -------------------------------------------------------------- softmax
-    const int t = (warp - 4) >> 2;    // query tile of this warpgroup
-    const int wq = warp & 3;          // TMEM lane quarter
-    const int r = wq * 32 + lane;     // query row within the tile
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + kColS0 + 128 * t;
-    const uint32_t tO = tmem + lane_base + kColO0 + 64 * t;
-    const uint32_t tP = tmem + lane_base + kColP0 + 64 * t;
-    const float sl2 = p.scale_log2;
-    uint32_t s_cnt = 0, pv_cnt = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
-      if (t >= w.ntiles) continue;
-      const int h = w.h0 + t;
-      const int row = w.q0 + r;  // relative to sequence start
-      float m_used = -INFINITY, l = 0.f;
-      if (p.sinks) {
-        m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
-        l = 1.f;
-      }
-      for (int j = 0; j < w.n_kv; ++j) {
-        const int kt = w.kv_lo + j;
-        ok = mbar_wait_warp(bar(kBarSFull + t), s_cnt & 1, wc, 9);
-        if (!ok) break;
-        ++s_cnt;
-        tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld_32x32b_x32(tS + 0, sr + 0);
-        tmem_ld_32x32b_x32(tS + 32, sr + 32);
-        tmem_ld_32x32b_x32(tS + 64, sr + 64);
-        tmem_ld_32x32b_x32(tS + 96, sr + 96);
-        tmem_wait_ld();
-        reg_fence<128>(sr);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSFree + t));
-        float s[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        const int kbase = kt * kTileN;
-        const bool edge = (kbase + kTileN - 1 > w.q0) ||
-                          (p.window > 0 && kbase < w.q0 + kTileM - p.window);
-        if (edge) {
-          const int hi_c = row - kbase;
-          const int lo_c = p.window > 0 ? row - p.window + 1 - kbase : -1;
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > hi_c || c < lo_c) s[c] = -INFINITY;
-        }
-        float mx = s[0];
-#pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float m_tile = mx * sl2;
-        float alpha = 1.f;
-        const bool need = m_tile > m_used + 8.f;
-        if (__any_sync(0xffffffffu, need)) {
-          if (m_tile > m_used) {
-            alpha = ex2_approx(m_used - m_tile);  // m_used = -inf gives 0
-            m_used = m_tile;
-          }
-        }
-        l *= alpha;
-        const float m_use = m_used == -INFINITY ? 0.f : m_used;
-        uint32_t pk[64];
-        float rs = 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
-          rs += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        l += rs;
-        if (j > 0) {
-          // O_t is stable and P_t reusable once PV_t(j-1) has completed.
-          ok = mbar_wait_warp(bar(kBarPVDone + t), pv_cnt & 1, wc, 10);
-          if (!ok) break;
-          ++pv_cnt;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            uint32_t o[64];
-            tmem_ld_32x32b_x32(tO, o);
-            tmem_ld_32x32b_x32(tO + 32, o + 32);
-            tmem_wait_ld();
-            reg_fence<64>(o);
-#pragma unroll
-            for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st_32x32b_x32(tO, o);
-            tmem_st_32x32b_x32(tO + 32, o + 32);
-          }
-        }
-        tmem_st_32x32b_x32(tP, pk);
-        tmem_st_32x32b_x32(tP + 32, pk + 32);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + t));
-      }
-      if (!ok) break;
-      // ------------------------------------------------------------ epilogue
-      ok = mbar_wait_warp(bar(kBarPVDone + t), pv_cnt & 1, wc, 10);
-      if (!ok) break;
-      ++pv_cnt;
-      tc_fence_after();
-      uint32_t o[64];
-      tmem_ld_32x32b_x32(tO, o);
-      tmem_ld_32x32b_x32(tO + 32, o + 32);
-      tmem_wait_ld();
-      reg_fence<64>(o);
-      if (row < w.len) {
-        const float inv = 1.f / l;
-        const size_t orow = (size_t)(w.start + row) * p.Hq + h;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-          dst[c] = v;
-        }
-        if (p.lse) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
-      }
-      tc_fence_before();
-    }
-  }
+  if (warp == 0 && lane == 0) role_producer(cx, &tmQ, &tmK, &tmV, p);
+  else if (warp == 1 && lane == 0) role_mma(cx, p);
+  else if (warp >= 4) role_softmax(cx, p, warp, lane);
 
   // ------------------------------------------------------------------ teardown
   __syncwarp();
@@ -425,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(cx.tmem, kTmemCols);
   }
 }
 

@@ -54,28 +54,35 @@ struct WaitCtl {
   uint64_t timeout_ns;
 };
 
-// Waits for completion of the phase with the given parity.  Gives up when the
+// Slow path of mbar_wait, entered after one failed try.  Gives up when the
 // CTA's abort flag is raised or after `timeout_ns`; on its own timeout it
 // records TSK_ERR_DEVICE_TIMEOUT (-7) and the site in the status word and
 // raises the abort flag.  Returns false when it gave up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                            int site) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    // try_wait itself suspends for a while before reporting failure, so the
+    // checks below run at a low rate.
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*c.abort_flag) return false;
-      if (globaltimer_ns() - t0 > c.timeout_ns) {
-        if (atomicCAS(c.status, 0, -7) == 0) {
-          c.status[1] = site;
-          c.status[2] = (int)blockIdx.x;
-        }
-        *c.abort_flag = 1;
-        __threadfence_block();
-        return false;
+    if (*c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > c.timeout_ns) {
+      if (atomicCAS(c.status, 0, -7) == 0) {
+        c.status[1] = site;
+        c.status[2] = (int)blockIdx.x;
       }
+      *c.abort_flag = 1;
+      __threadfence_block();
+      return false;
     }
   }
+}
+
+// Waits for completion of the phase with the given parity (bounded).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                          int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, site);
 }
 
 // ----------------------------------------------------------------- TMA
@@ -199,6 +206,37 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed fp32 pair arithmetic (two lanes of one 64-bit register pair).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

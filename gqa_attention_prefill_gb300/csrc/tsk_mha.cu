@@ -46,6 +46,7 @@ int g_ev_dev = -1;
 bool g_ev_recorded = false;
 
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits give up after 2 s
+int g_debug_stall = 0;
 
 tsk_status cuda_fail(cudaError_t e) {
   (void)cudaGetLastError();
@@ -249,6 +250,7 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
   p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
+  p.debug_stall = g_debug_stall;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   tsk::attention_fwd_kernel<<<grid, tsk::kThreads, tsk::kSmemBytes, stream>>>(tq, tk, tv, p);
@@ -312,10 +314,11 @@ tsk_status tsk_release(void) {
   return TSK_OK;
 }
 
-// Test hook: shortens the device-side bounded waits (nanoseconds; 0 restores 2 s).
-tsk_status tsk_debug_set_wait_timeout_ns(unsigned long long ns) {
+// Test hook: wait limit for later calls (0 = default 2 s) and stall injection.
+tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall) {
   std::lock_guard<std::mutex> lock(g_mu);
-  g_timeout_ns = ns ? ns : 2000000000ull;
+  g_timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+  g_debug_stall = stall ? 1 : 0;
   return TSK_OK;
 }
 

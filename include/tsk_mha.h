@@ -113,13 +113,15 @@ TSK_API int32_t tsk_kernels_per_call(void);
 TSK_API tsk_status tsk_release(void);
 
 /*
- * Test hook: sets the limit of every device-side bounded wait of later calls
- * (nanoseconds; 0 restores the default of 2 s).  With a tiny limit the
- * attention kernel gives up early, records TSK_ERR_DEVICE_TIMEOUT, drains its
- * in-flight copies and MMAs (those keep a 2 s limit), frees TMEM and returns,
- * leaving the outputs incomplete; the CUDA context stays usable.
+ * Test hook for the device-side bounded waits.  `timeout_ns` is the limit of
+ * every wait of later calls (0 restores the default of 2 s).  With `stall`
+ * non-zero, the TMA producer of every CTA first waits on a barrier that
+ * nothing signals, so each CTA runs into the limit: it records
+ * TSK_ERR_DEVICE_TIMEOUT in the stream's status word, stops its other roles,
+ * drains in-flight copies and MMAs (those keep a 2 s limit), frees TMEM and
+ * returns without writing the outputs.  The CUDA context stays usable.
  */
-TSK_API tsk_status tsk_debug_set_wait_timeout_ns(unsigned long long ns);
+TSK_API tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 TSK_API int32_t tsk_version(void);

@@ -114,16 +114,23 @@ def test_bad_seqlens_reported_on_device():
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
+    import time
+    import torch
     import gqa_attention_prefill_gb300 as pkg
     w = inputgen.make([4096] * 2, 16, 2, seed=12)
     d = parity.to_device(w)
-    pkg.tsk_debug_set_wait_timeout_ns(1)   # every wait that does not succeed at once gives up
+    pkg.tsk_debug_set_wait(20_000_000, stall=True)   # 20 ms limit, a wait nothing satisfies
     try:
+        t0 = time.time()
         out, lse = parity.run_gpu(w, d, check_status=False)
         st = pkg.tsk_get_device_status()
+        dt = time.time() - t0
     finally:
-        pkg.tsk_debug_set_wait_timeout_ns(0)
-    assert st == -7
+        pkg.tsk_debug_set_wait(0, stall=False)
+    assert st == -7, pkg.STATUS.get(st, st)
+    assert dt < 10.0
+    assert bool(torch.isnan(out.float()).all())   # nothing written
+    print(f"timeout reported after {dt * 1e3:.0f} ms")
     print(parity.check_full(w, label="after timeout"))   # context usable, results right again
 
 
