@@ -20,6 +20,7 @@ import os
 import threading
 
 __all__ = ["tsk_mha_prefill", "mha_prefill", "tsk_get_device_status", "tsk_status_string",
+           "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
            "tsk_version", "TskError", "library_path", "load_library"]
 
@@ -36,7 +37,16 @@ STATUS = {0: "TSK_OK", -1: "TSK_ERR_INVALID_ARG", -2: "TSK_ERR_UNSUPPORTED",
 class TskError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {STATUS.get(code, code)} ({tsk_status_string(code)})")
+        detail = tsk_last_error() if code in (-4, -5, -6) else ""
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({tsk_status_string(code)})"
+                         + (f" [{detail}]" if detail else ""))
+
+
+def tsk_last_error() -> str:
+    try:
+        return load_library().tsk_last_error().decode()
+    except Exception:
+        return ""
 
 
 def library_path() -> str:
@@ -63,6 +73,8 @@ def load_library():
         lib.tsk_mha_prefill.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
+        lib.tsk_last_error.argtypes = []
+        lib.tsk_last_error.restype = ctypes.c_char_p
         lib.tsk_get_device_status.argtypes = [P]
         lib.tsk_get_device_status.restype = ctypes.c_int
         lib.tsk_profile_enable.argtypes = [ctypes.c_int]

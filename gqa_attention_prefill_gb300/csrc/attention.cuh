@@ -44,7 +44,15 @@ namespace tsk {
 #endif
 constexpr int kStages = TSK_KV_STAGES;           // K/V ring depth
 constexpr float kRescaleThreshold = TSK_RESCALE_THRESHOLD;  // log2 units
-constexpr int kThreads = 384;
+#ifndef TSK_EMU
+#define TSK_EMU 0       // of every 4 column pairs, how many take exp2 on the FMA pipe
+#endif
+#ifndef TSK_PINGPONG
+#define TSK_PINGPONG 0  // alternate the two tiles' exponential phases
+#endif
+constexpr int kFirstSoftmaxWarp = 4;
+constexpr int kSoftmaxWarpsPerTile = 4;
+constexpr int kThreads = 32 * (kFirstSoftmaxWarp + 2 * kSoftmaxWarpsPerTile);
 constexpr int kHeadDim = 64;
 constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // 16 KB (also K/V tiles)
 constexpr uint32_t kSmemQ = 0;                           // 2 buffers x 2 tiles
@@ -54,7 +62,6 @@ constexpr uint32_t kSmemBytes = kSmemBar + 512 + 1024;   // barriers + slack for
 
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr unsigned long long kDrainTimeoutNs = 2000000000ull;  // in-flight work always finishes
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
@@ -84,16 +91,19 @@ enum : int {
   kBarSFree = 6 + 3 * kStages,  // [2]
   kBarPFull = 8 + 3 * kStages,  // [2]
   kBarPVDone = 10 + 3 * kStages,  // [2]
-  kBarDrain = 12 + 3 * kStages,
-  kBarNever = 13 + 3 * kStages,  // never signalled (stall injection)
-  kNumBars = 14 + 3 * kStages
+  kBarDrain = 12 + 3 * kStages,  // [2] one per MMA issuer
+  kBarNever = 14 + 3 * kStages,  // never signalled (stall injection)
+  kBarTurn = 15 + 3 * kStages,   // [2] exp-phase ping-pong
+  kNumBars = 17 + 3 * kStages
 };
+static_assert(8 * kNumBars + 8 <= 512, "barrier area");
 
 // mbar_wait for warps whose every lane polls: the result is made warp-uniform
 // so that the warp-collective tcgen05 instructions that follow never diverge.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                               int site) {
-  const bool ok = mbar_wait(bar, parity, c, site);
+template <class P>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int site, const P& p,
+                                               uint32_t abort_saddr) {
+  const bool ok = mbar_wait(bar, parity, site, p, abort_saddr);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -125,16 +135,10 @@ struct Ctx {
   uint32_t bar0;    // first mbarrier
   uint32_t tmem;    // TMEM base address
   int total_units;
-  WaitCtl wc;
+  uint32_t abort;   // shared address of the CTA's abort flag
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 };
 
-__device__ __forceinline__ WaitCtl drain_ctl(const WaitCtl& wc, int* dummy_abort) {
-  WaitCtl dc = wc;
-  dc.abort_flag = dummy_abort;
-  if (dc.timeout_ns < kDrainTimeoutNs) dc.timeout_ns = kDrainTimeoutNs;
-  return dc;
-}
 
 // TMA producer (one thread).
 __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* tmQ,
@@ -143,11 +147,11 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   // ------------------------------------------------------------ producer
   uint32_t q_iter = 0, kv_iter = 0;
   bool ok = true;
-  if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, cx.wc, 99);
+  if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     const int qb = q_iter & 1;
-    if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, cx.wc, 1);
+    if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, 1, p, cx.abort);
     if (!ok) break;
     mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), w.ntiles * kTileBytes);
     for (int t = 0; t < w.ntiles; ++t)
@@ -157,7 +161,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
       const int s = kv_iter % kStages;
       const uint32_t k = kv_iter / kStages;
-      if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, cx.wc, 2);
+      if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, 2, p, cx.abort);
       if (!ok) break;
       const int row = w.start + (w.kv_lo + j) * kTileN;
       const uint32_t kdst = cx.sbase + kSmemKV + s * 2 * kTileBytes;
@@ -169,110 +173,115 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   }
   // Drain: wait for the last load issued into every buffer so that no
   // copy is still in flight when the CTA exits (bounded, best effort).
-  int dummy_abort = 0;
-  const WaitCtl dc = drain_ctl(cx.wc, &dummy_abort);
   for (uint32_t i = (kv_iter > kStages ? kv_iter - kStages : 0); i < kv_iter; ++i) {
-    mbar_wait(cx.bar(kBarKFull + i % kStages), (i / kStages) & 1, dc, 11);
-    mbar_wait(cx.bar(kBarVFull + i % kStages), (i / kStages) & 1, dc, 12);
+    mbar_wait<true>(cx.bar(kBarKFull + i % kStages), (i / kStages) & 1, 11, p, cx.abort);
+    mbar_wait<true>(cx.bar(kBarVFull + i % kStages), (i / kStages) & 1, 12, p, cx.abort);
   }
   for (uint32_t i = (q_iter > 2 ? q_iter - 2 : 0); i < q_iter; ++i)
-    mbar_wait(cx.bar(kBarQFull + (i & 1)), (i >> 1) & 1, dc, 13);
+    mbar_wait<true>(cx.bar(kBarQFull + (i & 1)), (i >> 1) & 1, 13, p, cx.abort);
 
 }
 
 // tcgen05.mma issuer (one thread).
-__device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p) {
-  // ------------------------------------------------------------ MMA issuer
-  uint32_t q_iter = 0, kv_iter = 0;
-  uint32_t s_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
+// tcgen05.mma issuer for query tile t (one thread; tiles 0 and 1 have their
+// own issuers, so a slow softmax of one tile never holds back the other's
+// MMAs).  Per key tile j:
+//   S_t(j+1) = Q_t K_{j+1}^T   once K_{j+1} is loaded and the softmax has read S_t(j)
+//   O_t += P_t(j) V_j          once V_j is loaded and the softmax has written P_t(j)
+// Each issuer releases a K/V stage (and the Q buffer) with its own commit, so
+// those barriers count two arrivals; for a unit with one query tile the tile-0
+// issuer commits twice and the tile-1 issuer only advances its counters.
+__device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
+  uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
   bool ok = true;
+  const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
+  const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
+  const uint32_t a_p = cx.tmem + kColP0 + 64 * t;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     const int qb = q_iter & 1;
-    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, cx.wc, 3);
+    if (t >= w.ntiles) {  // this tile is idle in the unit
+      kv_iter += w.n_kv;
+      ++q_iter;
+      continue;
+    }
+    const int commits = w.ntiles == 1 ? 2 : 1;  // arrivals owed on the shared release barriers
+    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3, p, cx.abort);
     if (!ok) break;
-    tc_fence_after();
-    const uint32_t qaddr = cx.sbase + kSmemQ + 2 * qb * kTileBytes;
-    auto issue_s = [&](int t, int stage) {
-      const uint32_t a = qaddr + t * kTileBytes;
+    const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes;
+    auto issue_s = [&](int stage) {
       const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        mma_ss(cx.tmem + kColS0 + 128 * t, sdesc_sw128(a + 32 * kk), sdesc_sw128(b + 32 * kk),
-               kIdescQK, kk > 0 ? 1u : 0u);
+        mma_ss(d_s, sdesc_sw128(qaddr + 32 * kk), sdesc_sw128(b + 32 * kk), kIdescQK,
+               kk > 0 ? 1u : 0u);
       tc_commit(cx.bar(kBarSFull + t));
+      ++s_cnt;
     };
-    auto issue_pv = [&](int t, int stage, bool acc) {
-      const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes + kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTileN / 16; ++kk)
-        mma_ts(cx.tmem + kColO0 + 64 * t, cx.tmem + kColP0 + 64 * t + 8 * kk,
-               sdesc_sw128(b + 2048 * kk), kIdescPV, (acc || kk > 0) ? 1u : 0u);
-      tc_commit(cx.bar(kBarPVDone + t));
-    };
-    // S_t(0)
-    {
+    {  // S_t(0)
       const int s0 = kv_iter % kStages;
-      ok = mbar_wait(cx.bar(kBarKFull + s0), (kv_iter / kStages) & 1, cx.wc, 4);
+      ok = mbar_wait(cx.bar(kBarKFull + s0), (kv_iter / kStages) & 1, 4, p, cx.abort);
+      if (ok && s_cnt > 0) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5, p, cx.abort);
       if (!ok) break;
       tc_fence_after();
-      for (int t = 0; t < w.ntiles && ok; ++t) {
-        if (s_cnt[t] > 0) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt[t] - 1) & 1, cx.wc, 5);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(t, s0);
-        ++s_cnt[t];
-      }
+      issue_s(s0);
     }
     for (int j = 0; j < w.n_kv && ok; ++j) {
       const uint32_t cur = kv_iter + j;
       const int sc = cur % kStages;
-      const int sn = (cur + 1) % kStages;
       if (j + 1 < w.n_kv) {
-        // S_t(j+1) for both tiles first, so neither softmax waits on the other's P.
-        ok = mbar_wait(cx.bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, cx.wc, 6);
+        const int sn = (cur + 1) % kStages;
+        ok = mbar_wait(cx.bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, 6, p, cx.abort);
+        if (ok) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5, p, cx.abort);
         if (!ok) break;
         tc_fence_after();
-        for (int t = 0; t < w.ntiles; ++t) {
-          ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt[t] - 1) & 1, cx.wc, 5);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(t, sn);
-          ++s_cnt[t];
-        }
-        if (!ok) break;
+        issue_s(sn);
       }
-      ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStages) & 1, cx.wc, 7);
+      ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStages) & 1, 7, p, cx.abort);
+      if (ok) ok = mbar_wait(cx.bar(kBarPFull + t), p_cnt & 1, 8, p, cx.abort);
       if (!ok) break;
       tc_fence_after();
-      for (int t = 0; t < w.ntiles; ++t) {
-        ok = mbar_wait(cx.bar(kBarPFull + t), p_cnt[t] & 1, cx.wc, 8);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(t, sc, j > 0);
-        ++p_cnt[t];
-      }
-      if (!ok) break;
-      tc_commit(cx.bar(kBarKVEmpty + sc));
+      const uint32_t b = cx.sbase + kSmemKV + sc * 2 * kTileBytes + kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_ts(d_o, a_p + 8 * kk, sdesc_sw128(b + 2048 * kk), kIdescPV,
+               (j > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(cx.bar(kBarPVDone + t));
+      ++p_cnt;
+      for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarKVEmpty + sc));
     }
     if (!ok) break;
     kv_iter += w.n_kv;
-    tc_commit(cx.bar(kBarQEmpty + qb));
+    for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarQEmpty + qb));
     ++q_iter;
   }
-  // Make sure no MMA is still running before TMEM is freed.
-  tc_commit(cx.bar(kBarDrain));
-  int dummy_abort = 0;
-  const WaitCtl dc = drain_ctl(cx.wc, &dummy_abort);
-  mbar_wait(cx.bar(kBarDrain), 0, dc, 14);
-
+  // Make sure none of this thread's MMAs is still running before TMEM is freed.
+  tc_commit(cx.bar(kBarDrain + t));
+  mbar_wait<true>(cx.bar(kBarDrain + t), 0, 14, p, cx.abort);
 }
 
-// Softmax and epilogue of one query tile (one warpgroup, one thread per row).
+// Ping-pong of the two query tiles' exponential phases (the MUFU-bound part):
+// exp phase e of tile 1 starts after that of tile 0, and exp phase e+1 of
+// tile 0 after exp phase e of tile 1, so each runs with the special-function
+// units to itself while the other tile loads, reduces and stores.  Only units
+// with two active tiles take part; e counts those phases per tile.
+__device__ __forceinline__ bool turn_wait(const Ctx& cx, const AttnParams& p, int t, uint32_t e) {
+  if (t == 0) {
+    if (e == 0) return true;
+    return mbar_wait_warp(cx.bar(kBarTurn + 0), (e - 1) & 1, 17, p, cx.abort);
+  }
+  return mbar_wait_warp(cx.bar(kBarTurn + 1), e & 1, 17, p, cx.abort);
+}
+__device__ __forceinline__ void turn_pass(const Ctx& cx, int t, int lane, uint32_t& e) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(cx.bar(kBarTurn + (t ^ 1)));
+  ++e;
+}
+
 __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p, int warp,
                                           int lane) {
   // -------------------------------------------------------------- softmax
-  const int t = (warp - 4) >> 2;    // query tile of this warpgroup
+  const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;          // TMEM lane quarter
   const int r = wq * 32 + lane;     // query row within the tile
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -280,7 +289,8 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
   const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
   const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
   const float sl2 = p.scale_log2;
-  uint32_t s_cnt = 0, pv_cnt = 0;
+  uint32_t s_cnt = 0, pv_cnt = 0, e_cnt = 0;
+  TSK_TRACE_T0(tr_all);
   bool ok = true;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
@@ -294,10 +304,11 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
     }
     for (int j = 0; j < w.n_kv; ++j) {
       const int kt = w.kv_lo + j;
-      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, cx.wc, 9);
+      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, 9, p, cx.abort);
       if (!ok) break;
       ++s_cnt;
       tc_fence_after();
+      TSK_TRACE_T0(tr_ld);
       uint32_t sr[128];
       tmem_ld_32x32b_x32(tS + 0, sr + 0);
       tmem_ld_32x32b_x32(tS + 32, sr + 32);
@@ -305,6 +316,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
       tmem_ld_32x32b_x32(tS + 96, sr + 96);
       tmem_wait_ld();
       reg_fence<128>(sr);
+      TSK_TRACE_ADD(20, tr_ld);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
@@ -322,6 +334,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
           if (c > hi_c || c < lo_c) s[c] = -INFINITY;
       }
       // Row maximum: four independent chains of 3-input max.
+      TSK_TRACE_T0(tr_max);
       float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
 #pragma unroll
       for (int c = 4; c < 128; c += 8) {
@@ -331,6 +344,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
         m3 = max3f(m3, s[c + 6], s[c + 7]);
       }
       const float m_tile = max3f(m0, m1, fmaxf(m2, m3)) * sl2;
+      TSK_TRACE_ADD(21, tr_max);
       float alpha = 1.f;
       const bool need = m_tile > m_used + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
@@ -343,16 +357,25 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
       // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per
       // element, four packed partial sums, bf16x2 packing for TMEM.
+      if (TSK_PINGPONG && w.ntiles == 2) {
+        ok = turn_wait(cx, p, t, e_cnt);
+        if (!ok) break;
+      }
+      TSK_TRACE_T0(tr_exp);
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm = f2_pack(-m_use, -m_use);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        float x0, x1;
+        float x0, x1, p0, p1;
         f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm), x0, x1);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
+        if ((c & 3) < TSK_EMU) {
+          ex2_poly_pair(x0, x1, p0, p1);
+        } else {
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
+        }
         const uint64_t pp = f2_pack(p0, p1);
         acc[c & 3] = c < 4 ? pp : f2_add(acc[c & 3], pp);
         pk[c] = pack_bf16x2(p0, p1);
@@ -364,9 +387,11 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
         f2_unpack(f2_add(a01, a23), r0, r1);
         l += r0 + r1;
       }
+      TSK_TRACE_ADD(22, tr_exp);
+      if (TSK_PINGPONG && w.ntiles == 2) turn_pass(cx, t, lane, e_cnt);
       if (j > 0) {
         // O_t is stable and P_t reusable once PV_t(j-1) has completed.
-        ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, cx.wc, 10);
+        ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
         if (!ok) break;
         ++pv_cnt;
         tc_fence_after();
@@ -382,16 +407,18 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
           tmem_st_32x32b_x32(tO + 32, o + 32);
         }
       }
+      TSK_TRACE_T0(tr_st);
       tmem_st_32x32b_x32(tP, pk);
       tmem_st_32x32b_x32(tP + 32, pk + 32);
       tmem_wait_st();
+      TSK_TRACE_ADD(23, tr_st);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
     }
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
-    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, cx.wc, 10);
+    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
     if (!ok) break;
     ++pv_cnt;
     tc_fence_after();
@@ -418,6 +445,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
     tc_fence_before();
   }
 
+  TSK_TRACE_ADD(30, tr_all);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -440,18 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(cx.bar(kBarQFull + i), 1);
-      mbar_init(cx.bar(kBarQEmpty + i), 1);
+      mbar_init(cx.bar(kBarQEmpty + i), 2);
       mbar_init(cx.bar(kBarSFull + i), 1);
-      mbar_init(cx.bar(kBarSFree + i), 4);
-      mbar_init(cx.bar(kBarPFull + i), 4);
+      mbar_init(cx.bar(kBarSFree + i), kSoftmaxWarpsPerTile);
+      mbar_init(cx.bar(kBarTurn + i), kSoftmaxWarpsPerTile);
+      mbar_init(cx.bar(kBarPFull + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPVDone + i), 1);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(cx.bar(kBarKFull + s), 1);
       mbar_init(cx.bar(kBarVFull + s), 1);
-      mbar_init(cx.bar(kBarKVEmpty + s), 1);
+      mbar_init(cx.bar(kBarKVEmpty + s), 2);
     }
     mbar_init(cx.bar(kBarDrain), 1);
+    mbar_init(cx.bar(kBarDrain + 1), 1);
     mbar_init(cx.bar(kBarNever), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -465,16 +495,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  trace_init();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   cx.tmem = *tmem_slot;
-  cx.wc = WaitCtl{abort_flag, p.status, p.timeout_ns};
+  cx.abort = smem_u32(const_cast<int*>(abort_flag));
   cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
 
   if (warp == 0 && lane == 0) role_producer(cx, &tmQ, &tmK, &tmV, p);
-  else if (warp == 1 && lane == 0) role_mma(cx, p);
-  else if (warp >= 4) role_softmax(cx, p, warp, lane);
+  else if (warp == 1 && lane == 0) role_mma(cx, p, 0);
+  else if (warp == 2 && lane == 0) role_mma(cx, p, 1);
+  else if (warp >= kFirstSoftmaxWarp) role_softmax(cx, p, warp, lane);
 
   // ------------------------------------------------------------------ teardown
   __syncwarp();
@@ -484,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(cx.tmem, kTmemCols);
   }
+  trace_flush();
 }
 
 }  // namespace tsk

@@ -17,6 +17,39 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ----------------------------------------------------------------- tracing
+// Builds with -DTSK_TRACE accumulate clock64() cycles per code site (lane 0 of
+// each warp, in shared memory, flushed once at kernel exit) into
+// g_tsk_trace[site] and the number of visits into g_tsk_trace[kTraceSites +
+// site]; tsk_debug_trace() reads and clears them.
+constexpr int kTraceSites = 64;
+#ifdef TSK_TRACE
+__device__ unsigned long long g_tsk_trace[2 * kTraceSites];
+__shared__ unsigned long long s_tsk_trace[32][2 * kTraceSites];  // [warp][cycles | visits]
+#define TSK_TRACE_T0(v) const long long v = clock64()
+#define TSK_TRACE_ADD(site, t0)                                                   \
+  do {                                                                             \
+    if ((threadIdx.x & 31) == 0) {                                                 \
+      s_tsk_trace[threadIdx.x >> 5][(site)] += (unsigned long long)(clock64() - (t0)); \
+      s_tsk_trace[threadIdx.x >> 5][kTraceSites + (site)] += 1ull;                 \
+    }                                                                              \
+  } while (0)
+__device__ __forceinline__ void trace_init() {
+  for (int i = threadIdx.x; i < 32 * 2 * kTraceSites; i += blockDim.x) (&s_tsk_trace[0][0])[i] = 0;
+}
+__device__ __forceinline__ void trace_flush() {
+  for (int i = threadIdx.x; i < 32 * 2 * kTraceSites; i += blockDim.x) {
+    const unsigned long long v = (&s_tsk_trace[0][0])[i];
+    if (v) atomicAdd(&g_tsk_trace[i % (2 * kTraceSites)], v);
+  }
+}
+#else
+#define TSK_TRACE_T0(v)
+#define TSK_TRACE_ADD(site, t0)
+__device__ __forceinline__ void trace_init() {}
+__device__ __forceinline__ void trace_flush() {}
+#endif
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -47,42 +80,72 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Shared abort state of one CTA plus the device status word.
-struct WaitCtl {
-  volatile int* abort_flag;  // shared memory
-  int* status;               // global: [0] first error code, [1] site, [2] block
-  uint64_t timeout_ns;
-};
+// Non-blocking probe of a phase's completion.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
-// Slow path of mbar_wait, entered after one failed try.  Gives up when the
-// CTA's abort flag is raised or after `timeout_ns`; on its own timeout it
-// records TSK_ERR_DEVICE_TIMEOUT (-7) and the site in the status word and
-// raises the abort flag.  Returns false when it gave up.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                            int site) {
+// Bounded waits.  A CTA keeps an abort flag in shared memory; the device
+// status word and the time limit come from the kernel parameters (type P with
+// members `int* status` and `unsigned long long timeout_ns`), read only on the
+// slow path so that the fast path holds no extra registers.
+__device__ __forceinline__ int ld_shared_volatile(uint32_t a) {
+  int v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_volatile(uint32_t a, int v) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Slow path, entered after one failed try.  Unless `drain`, it gives up when
+// the CTA's abort flag is raised or after p.timeout_ns, recording
+// TSK_ERR_DEVICE_TIMEOUT (-7), the site and the block in p.status[0..2] and
+// raising the abort flag.  Drain waits (for work that is already in flight and
+// always finishes) ignore the flag and use a limit of at least 2 s.
+template <bool kDrain, class P>
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int site,
+                                               const P& p, uint32_t abort_saddr) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     // try_wait itself suspends for a while before reporting failure, so the
     // checks below run at a low rate.
     if (mbar_try_wait(bar, parity)) return true;
-    if (*c.abort_flag) return false;
-    if (globaltimer_ns() - t0 > c.timeout_ns) {
-      if (atomicCAS(c.status, 0, -7) == 0) {
-        c.status[1] = site;
-        c.status[2] = (int)blockIdx.x;
+    if (!kDrain && ld_shared_volatile(abort_saddr)) return false;
+    unsigned long long lim = p.timeout_ns;
+    if (kDrain && lim < 2000000000ull) lim = 2000000000ull;
+    if (globaltimer_ns() - t0 > lim) {
+      if (atomicCAS(p.status, 0, -7) == 0) {
+        p.status[1] = site;
+        p.status[2] = (int)blockIdx.x;
       }
-      *c.abort_flag = 1;
-      __threadfence_block();
+      st_shared_volatile(abort_saddr, 1);
       return false;
     }
   }
 }
 
 // Waits for completion of the phase with the given parity (bounded).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                          int site) {
+template <bool kDrain = false, class P>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int site, const P& p,
+                                          uint32_t abort_saddr) {
+#ifdef TSK_TRACE
+  TSK_TRACE_T0(t0);
+  const bool r =
+      mbar_try_wait(bar, parity) || mbar_wait_slow<kDrain>(bar, parity, site, p, abort_saddr);
+  TSK_TRACE_ADD(site, t0);
+  return r;
+#else
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, c, site);
+  return mbar_wait_slow<kDrain>(bar, parity, site, p, abort_saddr);
+#endif
 }
 
 // ----------------------------------------------------------------- TMA
@@ -237,6 +300,34 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+// 2^x for a pair on the FMA pipe instead of the MUFU: round x to the
+// nearest integer j with the 1.5*2^23 shifter, evaluate 2^f for f = x - j in
+// [-1/2, 1/2] by a cubic with constant term 1 (coefficients fitted here for
+// minimal relative error: max relative error 1.0e-4, far below the bf16
+// rounding of P), and add j to the exponent field with an integer
+// multiply-add.  x is clamped to -127 first, so -inf yields exactly +0.
+__device__ __forceinline__ void ex2_poly_pair(float x0, float x1, float& y0, float& y1) {
+  const uint64_t kShift = f2_pack(12582912.0f, 12582912.0f);  // 1.5 * 2^23
+  const uint64_t kNegShift = f2_pack(-12582912.0f, -12582912.0f);
+  const uint64_t kNegOne = f2_pack(-1.0f, -1.0f);
+  const uint64_t kC3 = f2_pack(0.05500893294811249f, 0.05500893294811249f);
+  const uint64_t kC2 = f2_pack(0.2422109693288803f, 0.2422109693288803f);
+  const uint64_t kC1 = f2_pack(0.6932829022407532f, 0.6932829022407532f);
+  const uint64_t kOne = f2_pack(1.0f, 1.0f);
+  const uint64_t x = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+  const uint64_t t = f2_add(x, kShift);           // low mantissa bits hold round(x)
+  const uint64_t j = f2_add(t, kNegShift);        // round(x), exact
+  const uint64_t f = f2_fma(j, kNegOne, x);       // x - round(x)
+  uint64_t q = f2_fma(f, kC3, kC2);
+  q = f2_fma(q, f, kC1);
+  q = f2_fma(q, f, kOne);
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t, t0, t1);
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -48,7 +48,15 @@ bool g_ev_recorded = false;
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits give up after 2 s
 int g_debug_stall = 0;
 
-tsk_status cuda_fail(cudaError_t e) {
+thread_local char g_last_error[256] = "";
+
+void note_error(const char* where, cudaError_t e) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+}
+
+tsk_status cuda_fail(cudaError_t e, const char* where = "CUDA call") {
+  note_error(where, e);
   (void)cudaGetLastError();
   return e == cudaErrorMemoryAllocation ? TSK_ERR_OOM : TSK_ERR_DEVICE;
 }
@@ -164,6 +172,27 @@ const char* tsk_status_string(tsk_status s) {
 
 int32_t tsk_version(void) { return kVersion; }
 
+const char* tsk_last_error(void) { return g_last_error; }
+
+tsk_status tsk_debug_trace(unsigned long long* out, int32_t n) {
+#ifdef TSK_TRACE
+  if (!out || n <= 0) return TSK_ERR_INVALID_ARG;
+  unsigned long long buf[2 * tsk::kTraceSites];
+  int m = n < 2 * tsk::kTraceSites ? n : 2 * tsk::kTraceSites;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(buf, tsk::g_tsk_trace, sizeof buf);
+  if (e != cudaSuccess) return cuda_fail(e, "trace read");
+  for (int i = 0; i < m; ++i) out[i] = buf[i];
+  unsigned long long zero[2 * tsk::kTraceSites] = {};
+  e = cudaMemcpyToSymbol(tsk::g_tsk_trace, zero, sizeof zero);
+  return e == cudaSuccess ? TSK_OK : cuda_fail(e, "trace clear");
+#else
+  (void)out;
+  (void)n;
+  return TSK_ERR_UNSUPPORTED;
+#endif
+}
+
 int32_t tsk_kernels_per_call(void) { return 2; }
 
 tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const float* sinks,
@@ -255,6 +284,7 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   tsk::attention_fwd_kernel<<<grid, tsk::kThreads, tsk::kSmemBytes, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) note_error("attention kernel launch", e);
   if (prof) {
     cudaEventRecord(g_ev[2], stream);
     g_ev_recorded = true;

@@ -89,6 +89,11 @@ TSK_API tsk_status tsk_mha_prefill(const void *q, const void *k, const void *v, 
 /* Human-readable name of a status code (static string). */
 TSK_API const char *tsk_status_string(tsk_status s);
 
+/* Text of the last CUDA error this library saw on the calling host thread
+ * ("" if none): which step failed and CUDA's error name and message.  The
+ * string stays valid until the next call on this thread. */
+TSK_API const char *tsk_last_error(void);
+
 /*
  * Synchronises `stream`, reads and clears the device status word of that
  * stream's workspace: TSK_OK, TSK_ERR_DEVICE_TIMEOUT (a bounded wait expired;
@@ -122,6 +127,16 @@ TSK_API tsk_status tsk_release(void);
  * returns without writing the outputs.  The CUDA context stays usable.
  */
 TSK_API tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall);
+
+/*
+ * Profiling hook of builds compiled with -DTSK_TRACE (returns
+ * TSK_ERR_UNSUPPORTED otherwise).  Synchronises the device and copies up to
+ * n counters into `out`: out[i] = clock cycles spent at code site i, summed
+ * over lane 0 of every warp that passed it, and out[64 + i] = the number of
+ * passes; then clears them.  Sites 1..15 are the bounded waits (numbered as
+ * the status word reports them), 20..23 softmax phases, 30 softmax total.
+ */
+TSK_API tsk_status tsk_debug_trace(unsigned long long *out, int32_t n);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 TSK_API int32_t tsk_version(void);

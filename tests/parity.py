@@ -37,7 +37,7 @@ def run_gpu(w: inputgen.Workload, d=None, with_lse=True, check_status=True):
         if with_lse else None
     rc = pkg.tsk_mha_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu"], w.num_seqs, T, w.Hq,
                              w.Hkv, w.D, w.window, w.scale, out, lse)
-    assert rc == 0, pkg.STATUS.get(rc, rc)
+    assert rc == 0, f"{pkg.STATUS.get(rc, rc)} {pkg.tsk_last_error()}"
     torch.cuda.synchronize()
     if check_status:
         st = pkg.tsk_get_device_status()
