@@ -1,32 +1,33 @@
 // Persistent, warp-specialised causal GQA attention forward for sm_103a.
 //
-// One CTA per SM walks a static stride over the work units of the sorted
-// query-tile list.  A unit is (query tile of 128 rows, KV head g, head pair):
-// two query heads of the same KV group over the same 128 tokens, so both
-// share every K/V tile staged in shared memory (GQA reuse) and have identical
-// key ranges.  Roles:
+// One CTA per SM walks a static stride over the work units of the query-tile
+// list, which the scheduler pre-pass sorted by cost (longest first).  A unit
+// is (query tile of 128 rows, KV head g, head pair): two query heads of the
+// same KV group over the same 128 tokens, so both share every K/V tile staged
+// in shared memory (GQA reuse) and have identical key ranges.  Roles:
 //   warp 0        TMA producer: Q tiles (2 x 16 KB, double buffered) and a
 //                 ring of kStages K/V stages (16 KB + 16 KB each)
-//   warp 1        allocates TMEM; one lane issues tcgen05.mma:
-//                   S_t = Q_t K_j^T   (M=128, N=128, K=64, both K-major, smem)
-//                   O_t += P_t V_j    (M=128, N=64,  K=128; P from TMEM, V MN-major)
+//   warp 1        allocates TMEM; one lane issues tile 0's tcgen05.mma:
+//                   S_0 = Q_0 K_j^T   (M=128, N=128, K=64, both K-major, smem)
+//                   O_0 += P_0 V_j    (M=128, N=64,  K=128; P from TMEM, V MN-major)
+//   warp 2        one lane issues tile 1's MMAs (same shapes)
 //   warps 4..7    softmax + epilogue for query tile t=0 (one thread per row)
 //   warps 8..11   softmax + epilogue for query tile t=1
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 //               P0 [384,448) P1 [448,512)  (P is bf16, two per column)
-// The MMA warp computes S_t(j+1) while the softmax of tile t works on S_t(j),
-// and the two tiles interleave on the tensor core.
+// The issuer of tile t computes S_t(j+1) while the softmax of tile t works on
+// S_t(j); the two tiles share the tensor core.
 //
 // Softmax (base 2): x = s * scale * log2(e).  The running maximum m and sum l
 // start from the sink (m = sink*log2 e, l = 1) or from (-inf, 0) without one.
 // The maximum used for exponentials is only raised when a tile's maximum
-// exceeds it by more than 8 (then O and l are rescaled); p <= 2^8 otherwise.
-// The result is exact up to rounding because the same m enters numerator and
-// denominator.  Only tiles that straddle the causal diagonal or the window's
-// lower edge evaluate the mask; tiles outside [kv_lo, diagonal] are never
-// visited.  Every wait is bounded (WaitCtl): on expiry the kernel records
-// TSK_ERR_DEVICE_TIMEOUT, stops all roles, drains its copies and MMAs, frees
-// TMEM and returns.
+// exceeds it by more than kRescaleThreshold (then O and l are rescaled); so
+// p <= 2^kRescaleThreshold.  The result is exact up to rounding because the
+// same m enters numerator and denominator.  Only tiles that straddle the
+// causal diagonal or the window's lower edge evaluate the mask; key tiles
+// outside [kv_lo, diagonal] are never visited.  Every wait is bounded: on
+// expiry the kernel records TSK_ERR_DEVICE_TIMEOUT, stops all roles, drains
+// its copies and MMAs, frees TMEM and returns.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -44,12 +45,6 @@ namespace tsk {
 #endif
 constexpr int kStages = TSK_KV_STAGES;           // K/V ring depth
 constexpr float kRescaleThreshold = TSK_RESCALE_THRESHOLD;  // log2 units
-#ifndef TSK_EMU
-#define TSK_EMU 0       // of every 4 column pairs, how many take exp2 on the FMA pipe
-#endif
-#ifndef TSK_PINGPONG
-#define TSK_PINGPONG 0  // alternate the two tiles' exponential phases
-#endif
 constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kSoftmaxWarpsPerTile = 4;
 constexpr int kThreads = 32 * (kFirstSoftmaxWarp + 2 * kSoftmaxWarpsPerTile);
@@ -93,8 +88,7 @@ enum : int {
   kBarPVDone = 10 + 3 * kStages,  // [2]
   kBarDrain = 12 + 3 * kStages,  // [2] one per MMA issuer
   kBarNever = 14 + 3 * kStages,  // never signalled (stall injection)
-  kBarTurn = 15 + 3 * kStages,   // [2] exp-phase ping-pong
-  kNumBars = 17 + 3 * kStages
+  kNumBars = 15 + 3 * kStages
 };
 static_assert(8 * kNumBars + 8 <= 512, "barrier area");
 
@@ -260,27 +254,9 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   mbar_wait<true>(cx.bar(kBarDrain + t), 0, 14, p, cx.abort);
 }
 
-// Ping-pong of the two query tiles' exponential phases (the MUFU-bound part):
-// exp phase e of tile 1 starts after that of tile 0, and exp phase e+1 of
-// tile 0 after exp phase e of tile 1, so each runs with the special-function
-// units to itself while the other tile loads, reduces and stores.  Only units
-// with two active tiles take part; e counts those phases per tile.
-__device__ __forceinline__ bool turn_wait(const Ctx& cx, const AttnParams& p, int t, uint32_t e) {
-  if (t == 0) {
-    if (e == 0) return true;
-    return mbar_wait_warp(cx.bar(kBarTurn + 0), (e - 1) & 1, 17, p, cx.abort);
-  }
-  return mbar_wait_warp(cx.bar(kBarTurn + 1), e & 1, 17, p, cx.abort);
-}
-__device__ __forceinline__ void turn_pass(const Ctx& cx, int t, int lane, uint32_t& e) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(cx.bar(kBarTurn + (t ^ 1)));
-  ++e;
-}
-
+// Softmax and epilogue of query tile t (one warpgroup, one thread per row).
 __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p, int warp,
                                           int lane) {
-  // -------------------------------------------------------------- softmax
   const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;          // TMEM lane quarter
   const int r = wq * 32 + lane;     // query row within the tile
@@ -289,7 +265,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
   const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
   const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
   const float sl2 = p.scale_log2;
-  uint32_t s_cnt = 0, pv_cnt = 0, e_cnt = 0;
+  uint32_t s_cnt = 0, pv_cnt = 0;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
@@ -355,40 +331,24 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
       }
       l *= alpha;
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
-      // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per
-      // element, four packed partial sums, bf16x2 packing for TMEM.
-      if (TSK_PINGPONG && w.ntiles == 2) {
-        ok = turn_wait(cx, p, t, e_cnt);
-        if (!ok) break;
-      }
       TSK_TRACE_T0(tr_exp);
+      // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per element,
+      // four scalar partial sums, bf16x2 packing for TMEM.
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm = f2_pack(-m_use, -m_use);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        float x0, x1, p0, p1;
+        float x0, x1;
         f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm), x0, x1);
-        if ((c & 3) < TSK_EMU) {
-          ex2_poly_pair(x0, x1, p0, p1);
-        } else {
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
-        }
-        const uint64_t pp = f2_pack(p0, p1);
-        acc[c & 3] = c < 4 ? pp : f2_add(acc[c & 3], pp);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        acc[c & 3] += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      {
-        const uint64_t a01 = f2_add(acc[0], acc[1]);
-        const uint64_t a23 = f2_add(acc[2], acc[3]);
-        float r0, r1;
-        f2_unpack(f2_add(a01, a23), r0, r1);
-        l += r0 + r1;
-      }
+      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       TSK_TRACE_ADD(22, tr_exp);
-      if (TSK_PINGPONG && w.ntiles == 2) turn_pass(cx, t, lane, e_cnt);
       if (j > 0) {
         // O_t is stable and P_t reusable once PV_t(j-1) has completed.
         ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
@@ -471,7 +431,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(cx.bar(kBarQEmpty + i), 2);
       mbar_init(cx.bar(kBarSFull + i), 1);
       mbar_init(cx.bar(kBarSFree + i), kSoftmaxWarpsPerTile);
-      mbar_init(cx.bar(kBarTurn + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPFull + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPVDone + i), 1);
     }

@@ -302,34 +302,6 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
-// 2^x for a pair on the FMA pipe instead of the MUFU: round x to the
-// nearest integer j with the 1.5*2^23 shifter, evaluate 2^f for f = x - j in
-// [-1/2, 1/2] by a cubic with constant term 1 (coefficients fitted here for
-// minimal relative error: max relative error 1.0e-4, far below the bf16
-// rounding of P), and add j to the exponent field with an integer
-// multiply-add.  x is clamped to -127 first, so -inf yields exactly +0.
-__device__ __forceinline__ void ex2_poly_pair(float x0, float x1, float& y0, float& y1) {
-  const uint64_t kShift = f2_pack(12582912.0f, 12582912.0f);  // 1.5 * 2^23
-  const uint64_t kNegShift = f2_pack(-12582912.0f, -12582912.0f);
-  const uint64_t kNegOne = f2_pack(-1.0f, -1.0f);
-  const uint64_t kC3 = f2_pack(0.05500893294811249f, 0.05500893294811249f);
-  const uint64_t kC2 = f2_pack(0.2422109693288803f, 0.2422109693288803f);
-  const uint64_t kC1 = f2_pack(0.6932829022407532f, 0.6932829022407532f);
-  const uint64_t kOne = f2_pack(1.0f, 1.0f);
-  const uint64_t x = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
-  const uint64_t t = f2_add(x, kShift);           // low mantissa bits hold round(x)
-  const uint64_t j = f2_add(t, kNegShift);        // round(x), exact
-  const uint64_t f = f2_fma(j, kNegOne, x);       // x - round(x)
-  uint64_t q = f2_fma(f, kC3, kC2);
-  q = f2_fma(q, f, kC1);
-  q = f2_fma(q, f, kOne);
-  float q0, q1, t0, t1;
-  f2_unpack(q, q0, q1);
-  f2_unpack(t, t0, t1);
-  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
-  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
