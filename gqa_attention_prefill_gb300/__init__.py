@@ -19,7 +19,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["tsk_mha_prefill", "mha_prefill", "tsk_get_device_status", "tsk_status_string",
+__all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "mha_prefill", "tsk_get_device_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
            "tsk_version", "TskError", "library_path", "load_library"]
@@ -71,6 +71,8 @@ def load_library():
         lib.tsk_mha_prefill.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32,
                                         ctypes.c_float, P, P, P]
         lib.tsk_mha_prefill.restype = ctypes.c_int
+        lib.tsk_mha_prefill_noalloc.argtypes = lib.tsk_mha_prefill.argtypes
+        lib.tsk_mha_prefill_noalloc.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
         lib.tsk_last_error.argtypes = []
@@ -128,6 +130,20 @@ def tsk_mha_prefill(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, Hq, Hkv,
                                int(num_seqs), int(total_tokens), int(Hq), int(Hkv), int(D),
                                int(window), float(scale), _ptr(out), _ptr(lse),
                                _stream_handle(stream))
+
+
+def tsk_mha_prefill_noalloc(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, Hq, Hkv, D,
+                            window, scale, out, lse, stream=None) -> int:
+    """Allocation-free variant (same arguments as ``tsk_mha_prefill``): its
+    scratch is a fixed array inside the library, for callers that may not
+    allocate device memory while running.  Calls that overlap on the GPU
+    race on that shared array; problems beyond its limits return
+    TSK_ERR_UNSUPPORTED."""
+    lib = load_library()
+    return lib.tsk_mha_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens),
+                                       int(num_seqs), int(total_tokens), int(Hq), int(Hkv),
+                                       int(D), int(window), float(scale), _ptr(out), _ptr(lse),
+                                       _stream_handle(stream))
 
 
 def mha_prefill(q, k, v, cu_seqlens, sinks=None, window: int = 0, scale: float | None = None,

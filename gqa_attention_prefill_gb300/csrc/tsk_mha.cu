@@ -353,3 +353,120 @@ tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.
+//
+// Some callers must not allocate device memory at call time: code running
+// under an allocator they do not control (a serving engine that owns the
+// whole memory pool), real-time paths where cudaMalloc's implicit
+// synchronisation is unacceptable, or hosts that forbid allocation after
+// start-up.  For them, tsk_mha_prefill_noalloc keeps its scratch (status
+// words, per-sequence tile offsets, sorted query-tile list) in the
+// file-scope array below, which every GPU that loads this library holds
+// until the process exits.  Its device address is looked up once per device
+// (cudaGetSymbolAddress on the first call made with that device current).
+namespace {
+
+constexpr int kNoAllocMaxSeqs = 16384;    // sequences per call
+constexpr int kNoAllocMaxTiles = 49152;   // total_tokens/128 + num_seqs + 1, at most
+constexpr size_t kNoAllocOffInts =
+    ((size_t)tsk::kWsHeader + (size_t)kNoAllocMaxSeqs + 1 + 3) & ~(size_t)3;
+constexpr size_t kNoAllocBytes = kNoAllocOffInts * 4 + (size_t)kNoAllocMaxTiles * 16;  // ~0.85 MB
+
+static __device__ __align__(256) int g_noalloc_scratch[kNoAllocBytes / 4];
+
+std::map<int, int*> g_noalloc_ptr;  // device -> device address of g_noalloc_scratch
+
+}  // namespace
+
+extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, const void* v,
+                                              const float* sinks, const int32_t* cu_seqlens,
+                                              int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                              int32_t Hkv, int32_t D, int32_t window,
+                                              float scale, void* out, float* lse,
+                                              tsk_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // Same host-side checks as tsk_mha_prefill, plus the scratch limits.
+  if (!q || !k || !v || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
+  if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
+    return TSK_ERR_UNSUPPORTED;
+  const int64_t max_tiles64 = total_tokens / tsk::kTileM + num_seqs + 1;
+  if (num_seqs > kNoAllocMaxSeqs || max_tiles64 > kNoAllocMaxTiles) {
+    snprintf(g_last_error, sizeof g_last_error,
+             "tsk_mha_prefill_noalloc: problem exceeds the fixed scratch (num_seqs %d > %d or "
+             "total_tokens/128 + num_seqs + 1 = %lld > %d)",
+             num_seqs, kNoAllocMaxSeqs, (long long)max_tiles64, kNoAllocMaxTiles);
+    return TSK_ERR_UNSUPPORTED;
+  }
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
+  if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return TSK_ERR_ALIGNMENT;
+  if (!a4(cu_seqlens) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
+  const size_t qo_bytes = (size_t)total_tokens * Hq * D * 2;
+  const size_t kv_bytes = (size_t)total_tokens * Hkv * D * 2;
+  if (total_tokens > 0 && (overlaps(out, qo_bytes, q, qo_bytes) ||
+                           overlaps(out, qo_bytes, k, kv_bytes) ||
+                           overlaps(out, qo_bytes, v, kv_bytes)))
+    return TSK_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  DeviceState* ds = nullptr;
+  tsk_status st = check_device(&dev, &ds);
+  if (st != TSK_OK) return st;
+  if ((st = get_encoder()) != TSK_OK) return st;
+  int*& scratch = g_noalloc_ptr[dev];
+  if (!scratch) {
+    // The array's name is a host-side stand-in; the device address must be
+    // looked up with this device current.
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    scratch = static_cast<int*>(ptr);
+  }
+
+  CUtensorMap tq, tk, tv;
+  if ((st = encode_thd(&tq, q, total_tokens, Hq)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, total_tokens, Hkv)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, total_tokens, Hkv)) != TSK_OK) return st;
+
+  int* tile_off = scratch + tsk::kWsHeader;
+  int4* list = reinterpret_cast<int4*>(scratch + kNoAllocOffInts);
+  // The array keeps the previous call's contents; the status words and the
+  // tile count must start at zero.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, tsk::kWsHeader * sizeof(int), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch header");
+  tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
+      cu_seqlens, num_seqs, (int)total_tokens, window, scratch, tile_off, list,
+      kNoAllocMaxTiles);
+
+  tsk::AttnParams p;
+  p.sinks = sinks;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.list = list;
+  p.ws = scratch;
+  p.status = scratch + tsk::kWsStatus;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.HP = (p.G + 1) / 2;
+  p.window = window;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.debug_stall = 0;
+  const int64_t units_bound = max_tiles64 * Hkv * p.HP;
+  const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
+  tsk::attention_fwd_kernel<<<grid, tsk::kThreads, tsk::kSmemBytes, stream>>>(tq, tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    note_error("attention kernel launch (no-alloc)", e);
+    return TSK_ERR_LAUNCH;
+  }
+  return TSK_OK;
+}

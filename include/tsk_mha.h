@@ -138,6 +138,36 @@ TSK_API tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall);
  */
 TSK_API tsk_status tsk_debug_trace(unsigned long long *out, int32_t n);
 
+/*
+ * tsk_mha_prefill_noalloc -- the same operation and arguments as
+ * tsk_mha_prefill, for callers that must not allocate device memory during a
+ * call: code running under a memory pool it does not own (a serving engine
+ * that has reserved the whole device), latency-critical paths where an
+ * allocation's implicit synchronisation is not acceptable, or processes that
+ * forbid allocation after start-up.  (The pages have no counterpart of this
+ * entry point; it is an addition of this library.)
+ *
+ * It calls no cudaMalloc/cudaFree or other allocating routine.  Its scratch
+ * (status words, tile offsets, the sorted query-tile list) is a fixed
+ * ~0.85 MB array in the library's device memory, which every GPU that loads
+ * the library holds until the process exits.  Limits: num_seqs <= 16384 and
+ * total_tokens/128 + num_seqs + 1 <= 49152; larger problems are rejected with
+ * TSK_ERR_UNSUPPORTED (tsk_last_error says which limit) before anything is
+ * enqueued.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array: calls whose
+ * work overlaps on the GPU (different streams, or host threads issuing
+ * concurrently) race and must be serialised by the caller.  Each call clears
+ * the status words it needs; device-side errors it detects (inconsistent
+ * cu_seqlens, an expired bounded wait) leave the outputs unwritten but are
+ * not reported by tsk_get_device_status.
+ */
+TSK_API tsk_status tsk_mha_prefill_noalloc(const void *q, const void *k, const void *v,
+                                           const float *sinks, const int32_t *cu_seqlens,
+                                           int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                           int32_t Hkv, int32_t D, int32_t window, float scale,
+                                           void *out, float *lse, tsk_stream_t stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 TSK_API int32_t tsk_version(void);
 
