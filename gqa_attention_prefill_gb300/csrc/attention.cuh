@@ -52,8 +52,11 @@ constexpr int kHeadDim = 64;
 constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // 16 KB (also K/V tiles)
 constexpr uint32_t kSmemQ = 0;                           // 2 buffers x 2 tiles
 constexpr uint32_t kSmemKV = 4 * kTileBytes;             // kStages x (K, V)
-constexpr uint32_t kSmemBar = kSmemKV + kStages * 2 * kTileBytes;
-constexpr uint32_t kSmemBytes = kSmemBar + 512 + 1024;   // barriers + slack for 1 KB alignment
+constexpr uint32_t kSmemBar = kSmemKV + kStages * 2 * kTileBytes;  // barriers (< 512 B)
+constexpr uint32_t kSmemEpi = kSmemBar + 1024;  // 2 output staging tiles (small-window kernel)
+// Dynamic shared memory per kernel variant, + 1 KB slack for the alignment.
+constexpr uint32_t kSmemBytesCausal = kSmemBar + 512 + 1024;
+constexpr uint32_t kSmemBytesWindow = kSmemEpi + 2 * kTileBytes + 1024;
 
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
 constexpr uint32_t kTmemCols = 512;
@@ -254,9 +257,39 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   mbar_wait<true>(cx.bar(kBarDrain + t), 0, 14, p, cx.abort);
 }
 
-// Softmax and epilogue of query tile t (one warpgroup, one thread per row).
-__device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p, int warp,
-                                          int lane) {
+// Column chunks of a 128-key tile (32 keys each) classified for one warp:
+// every row of the warp sees all keys of the chunk, none of them, or some.
+struct ChunkMask {
+  uint32_t none;     // bit k: chunk k masked for every row of the warp
+  uint32_t partial;  // bit k: chunk k needs a per-element test
+};
+
+// Allowed keys of query row `row` (relative to the sequence start) in the key
+// tile starting at `kbase`: columns c with lo_c <= c <= hi_c, where
+// hi_c = row - kbase and lo_c = row - window + 1 - kbase (window > 0).  The
+// warp's rows are row0 .. row0 + 31, so the bounds of its lanes 0 and 31
+// decide each chunk uniformly.
+__device__ __forceinline__ ChunkMask classify_chunks(int row0, int kbase, int window) {
+  ChunkMask m{0u, 0u};
+  const int hi_min = row0 - kbase, hi_max = hi_min + 31;
+  const int lo_min = window > 0 ? hi_min - window + 1 : -(1 << 30);
+  const int lo_max = window > 0 ? lo_min + 31 : -(1 << 30);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c0 = 32 * k, c1 = 32 * k + 31;
+    if (c1 < lo_min || c0 > hi_max) m.none |= 1u << k;
+    else if (!(c0 >= lo_max && c1 <= hi_min)) m.partial |= 1u << k;
+  }
+  return m;
+}
+
+// Softmax and epilogue of query tile t (one warpgroup, one thread per row),
+// used for full causal attention and windows wider than kSmallWindowMax:
+// each row's 128 scores are held in registers for one pass (maximum, then
+// exponentials), edge tiles are masked per element, and each thread stores
+// its output row directly.
+__device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnParams& p,
+                                                    int warp, int lane) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;          // TMEM lane quarter
   const int r = wq * 32 + lane;     // query row within the tile
@@ -408,10 +441,234 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
   TSK_TRACE_ADD(30, tr_all);
 }
 
+// Softmax and epilogue of query tile t (one warpgroup, one thread per row)
+// for sliding windows of at most kSmallWindowMax keys, where every query tile
+// visits only a few key tiles and per-tile costs dominate.  Each row's 128
+// scores are processed as two 64-column halves; 32-key chunks are classified
+// per warp so that only partly visible chunks pay a per-element mask.
+// Epilogue: the row is normalised, packed to bf16 and written into the warp's
+// 32-row slice of a 128-byte swizzled staging tile in shared memory; lane 0
+// stores the slice with one TMA bulk tensor store (box 64 x 1 x 32).  Warps
+// whose rows run past the end of their sequence (rows beyond it belong to the
+// next sequence) use direct per-row stores instead.
+__device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnParams& p,
+                                                    const CUtensorMap* tmO, int warp, int lane) {
+  const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
+  const int wq = warp & 3;                         // TMEM lane quarter
+  const int r = wq * 32 + lane;                    // query row within the tile
+  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  const uint32_t tS = cx.tmem + lane_base + kColS0 + 128 * t;
+  const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
+  const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
+  const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
+  const float sl2 = p.scale_log2;
+  uint32_t s_cnt = 0, pv_cnt = 0;
+  TSK_TRACE_T0(tr_all);
+  bool ok = true;
+  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    if (t >= w.ntiles) continue;
+    const int h = w.h0 + t;
+    const int row = w.q0 + r;  // relative to sequence start
+    float m_used = -INFINITY, l = 0.f;
+    if (p.sinks) {
+      m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
+      l = 1.f;
+    }
+    for (int j = 0; j < w.n_kv; ++j) {
+      const int kt = w.kv_lo + j;
+      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort);
+      if (!ok) break;
+      ++s_cnt;
+      tc_fence_after();
+      const int kbase = kt * kTileN;
+      const bool edge = (kbase + kTileN - 1 > w.q0) ||
+                        (p.window > 0 && kbase < w.q0 + kTileM - p.window);
+      ChunkMask cm{0u, 0u};
+      if (edge) cm = classify_chunks(w.q0 + wq * 32, kbase, p.window);
+      const int hi_c = row - kbase;
+      const int lo_c = p.window > 0 ? row - p.window + 1 - kbase : -1;
+      // The row's 128 scores are processed as two halves of 64 columns, so
+      // that at most one half of scores and the packed P of the other are
+      // held in registers at a time.
+      float alpha = 1.f;      // factor for O (both halves' rescales)
+      uint32_t pk[64];        // packed bf16 P of the row
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        TSK_TRACE_T0(tr_ld);
+        uint32_t sr[64];
+        tmem_ld_32x32b_x32(tS + 64 * hf, sr);
+        tmem_ld_32x32b_x32(tS + 64 * hf + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence<64>(sr);
+        TSK_TRACE_ADD(20, tr_ld);
+        if (hf == 1) {
+          // Both halves are in registers: the MMA may overwrite S_t.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
+        }
+        float sv[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(sr[c]);
+        // Mask: only chunks (32 keys) partly visible to this warp need a
+        // per-element test; chunks hidden from the whole warp are excluded
+        // from the maximum and get p = 0 through their offset below.
+        TSK_TRACE_T0(tr_mask);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int k = 2 * hf + kk;
+          if (cm.partial & (1u << k)) {
+#pragma unroll
+            for (int c = 32 * kk; c < 32 * kk + 32; ++c)
+              sv[c] = (64 * hf + c > hi_c || 64 * hf + c < lo_c) ? -INFINITY : sv[c];
+          }
+        }
+        TSK_TRACE_ADD(27, tr_mask);
+        TSK_TRACE_T0(tr_max);
+        float mk[2];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const float* v = sv + 32 * kk;
+          float a0 = v[0], a1 = v[1];
+#pragma unroll
+          for (int c = 2; c < 30; c += 4) {  // columns 2..29 of the chunk
+            a0 = max3f(a0, v[c], v[c + 1]);
+            a1 = max3f(a1, v[c + 2], v[c + 3]);
+          }
+          mk[kk] = max3f(a0, a1, fmaxf(v[30], v[31]));
+          if (cm.none & (1u << (2 * hf + kk))) mk[kk] = -INFINITY;
+        }
+        const float m_half = fmaxf(mk[0], mk[1]) * sl2;
+        TSK_TRACE_ADD(21, tr_max);
+        // Raise the maximum in use only when this half exceeds it by more
+        // than the threshold (then l, O and an already packed first half
+        // are rescaled; p <= 2^threshold otherwise).
+        if (__any_sync(0xffffffffu, m_half > m_used + kRescaleThreshold)) {
+          float beta = 1.f;
+          if (m_half > m_used) {
+            beta = ex2_approx(m_used - m_half);  // m_used = -inf gives 0
+            m_used = m_half;
+          }
+          l *= beta;
+          alpha *= beta;
+          if (hf == 1 && __any_sync(0xffffffffu, beta != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float lo = __uint_as_float(pk[c] << 16) * beta;
+              const float hi = __uint_as_float(pk[c] & 0xFFFF0000u) * beta;
+              pk[c] = pack_bf16x2(lo, hi);
+            }
+          }
+        }
+        const float m_use = m_used == -INFINITY ? 0.f : m_used;
+        // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per
+        // element, four scalar partial sums, bf16x2 packing.
+        TSK_TRACE_T0(tr_exp);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        uint64_t negm[2];  // -m, or -inf for chunks hidden from the whole warp
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const float nm = (cm.none & (1u << (2 * hf + kk))) ? -INFINITY : -m_use;
+          negm[kk] = f2_pack(nm, nm);
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sl2x2, negm[c >> 4]), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[c & 3] += p0 + p1;
+          pk[32 * hf + c] = pack_bf16x2(p0, p1);
+        }
+        l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        TSK_TRACE_ADD(22, tr_exp);
+      }
+      if (j > 0) {
+        // O_t is stable and P_t reusable once PV_t(j-1) has completed.
+        ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
+        if (!ok) break;
+        ++pv_cnt;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + 32 * hc, o);
+            tmem_wait_ld();
+            reg_fence<32>(o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st_32x32b_x32(tO + 32 * hc, o);
+          }
+        }
+      }
+      TSK_TRACE_T0(tr_st);
+      tmem_st_32x32b_x32(tP, pk);
+      tmem_st_32x32b_x32(tP + 32, pk + 32);
+      tmem_wait_st();
+      TSK_TRACE_ADD(23, tr_st);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
+    }
+    if (!ok) break;
+    // ------------------------------------------------------------ epilogue
+    TSK_TRACE_T0(tr_epi);
+    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
+    if (!ok) break;
+    ++pv_cnt;
+    tc_fence_after();
+    uint32_t o[64];
+    tmem_ld_32x32b_x32(tO, o);
+    tmem_ld_32x32b_x32(tO + 32, o + 32);
+    tmem_wait_ld();
+    reg_fence<64>(o);
+    const float inv = rcp_approx(l);
+    uint32_t ob[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+    const size_t orow = (size_t)(w.start + row) * p.Hq + h;
+    if (p.lse && row < w.len) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    if (w.q0 + wq * 32 + 32 <= w.len) {
+      // The warp's 32 rows lie inside the sequence: stage them in this warp's
+      // slice of the staging tile and store them with one TMA bulk store.
+      if (lane == 0) bulk_wait_group_read0();  // the warp's previous store has read its slice
+      __syncwarp();
+      const uint32_t dst_row = epi + (uint32_t)r * 128u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(dst_row + ((uint32_t)(c ^ (r & 7)) << 4), ob[4 * c], ob[4 * c + 1],
+                     ob[4 * c + 2], ob[4 * c + 3]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, w.start + w.q0 + wq * 32);
+        bulk_commit_group();
+      }
+    } else if (row < w.len) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+    }
+    tc_fence_before();
+    TSK_TRACE_ADD(28, tr_epi);
+  }
+  if (lane == 0) bulk_wait_group0();  // every output store of this warp has completed
+  TSK_TRACE_ADD(30, tr_all);
+}
+
+// kSmallWindow selects the softmax role for 0 < window <= kSmallWindowMax.
+constexpr int kSmallWindowMax = 512;
+
+template <bool kSmallWindow>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmO,
                          const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -449,12 +706,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   trace_init();
+  trace_cta_start();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -465,7 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) role_producer(cx, &tmQ, &tmK, &tmV, p);
   else if (warp == 1 && lane == 0) role_mma(cx, p, 0);
   else if (warp == 2 && lane == 0) role_mma(cx, p, 1);
-  else if (warp >= kFirstSoftmaxWarp) role_softmax(cx, p, warp, lane);
+  else if (warp >= kFirstSoftmaxWarp) {
+    if constexpr (kSmallWindow) role_softmax_window(cx, p, &tmO, warp, lane);
+    else role_softmax_causal(cx, p, warp, lane);
+  }
 
   // ------------------------------------------------------------------ teardown
   __syncwarp();
@@ -476,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(cx.tmem, kTmemCols);
   }
   trace_flush();
+  trace_cta_time();
 }
 
 }  // namespace tsk

@@ -43,11 +43,23 @@ __device__ __forceinline__ void trace_flush() {
     if (v) atomicAdd(&g_tsk_trace[i % (2 * kTraceSites)], v);
   }
 }
+// Per-CTA run time (globaltimer ns) of the last launch, by block index.
+constexpr int kTraceCtas = 1024;
+__device__ unsigned long long g_tsk_cta_ns[kTraceCtas];
+__shared__ unsigned long long s_tsk_t0;
+__device__ __forceinline__ void trace_cta_start() {
+  if (threadIdx.x == 0) s_tsk_t0 = globaltimer_ns();
+}
+__device__ __forceinline__ void trace_cta_time() {
+  if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_tsk_cta_ns[blockIdx.x] = globaltimer_ns() - s_tsk_t0;
+}
 #else
 #define TSK_TRACE_T0(v)
 #define TSK_TRACE_ADD(site, t0)
 __device__ __forceinline__ void trace_init() {}
 __device__ __forceinline__ void trace_flush() {}
+__device__ __forceinline__ void trace_cta_start() {}
+__device__ __forceinline__ void trace_cta_time() {}
 #endif
 
 // ----------------------------------------------------------------- mbarrier
@@ -162,6 +174,38 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// 3-D tiled store from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All committed bulk stores of this thread have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// All committed bulk stores of this thread have completed.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -268,6 +312,12 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 

@@ -72,12 +72,12 @@ tsk_status get_encoder() {
   return TSK_OK;
 }
 
-// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token); box = 64 x 1 x 128
-// rows of 128 bytes, stored with the 128-byte swizzle.
-tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H) {
+// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token); box = 64 x 1 x
+// box_rows rows of 128 bytes, stored with the 128-byte swizzle.
+tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int box_rows = 128) {
   cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {64 * 2, (cuuint64_t)H * 64 * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -106,9 +106,13 @@ tsk_status check_device(int* dev_out, DeviceState** st_out) {
   }
   if (!st.supported) return TSK_ERR_DEVICE;
   if (!st.smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(tsk::attention_fwd_kernel,
+    cudaError_t e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tsk::kSmemBytes);
+                                         (int)tsk::kSmemBytesCausal);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::kSmemBytesWindow);
     if (e != cudaSuccess) return cuda_fail(e);
     st.smem_set = true;
   }
@@ -177,13 +181,15 @@ const char* tsk_last_error(void) { return g_last_error; }
 tsk_status tsk_debug_trace(unsigned long long* out, int32_t n) {
 #ifdef TSK_TRACE
   if (!out || n <= 0) return TSK_ERR_INVALID_ARG;
-  unsigned long long buf[2 * tsk::kTraceSites];
-  int m = n < 2 * tsk::kTraceSites ? n : 2 * tsk::kTraceSites;
+  constexpr int kSites = 2 * tsk::kTraceSites;
+  unsigned long long buf[kSites + tsk::kTraceCtas];
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(buf, tsk::g_tsk_trace, sizeof buf);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(buf, tsk::g_tsk_trace, kSites * 8);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(buf + kSites, tsk::g_tsk_cta_ns, tsk::kTraceCtas * 8);
   if (e != cudaSuccess) return cuda_fail(e, "trace read");
+  const int m = n < kSites + tsk::kTraceCtas ? n : kSites + tsk::kTraceCtas;
   for (int i = 0; i < m; ++i) out[i] = buf[i];
-  unsigned long long zero[2 * tsk::kTraceSites] = {};
+  unsigned long long zero[kSites] = {};
   e = cudaMemcpyToSymbol(tsk::g_tsk_trace, zero, sizeof zero);
   return e == cudaSuccess ? TSK_OK : cuda_fail(e, "trace clear");
 #else
@@ -231,10 +237,11 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
   Workspace* ws = nullptr;
   if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((st = encode_thd(&tq, q, total_tokens, Hq)) != TSK_OK) return st;
   if ((st = encode_thd(&tk, k, total_tokens, Hkv)) != TSK_OK) return st;
   if ((st = encode_thd(&tv, v, total_tokens, Hkv)) != TSK_OK) return st;
+  if ((st = encode_thd(&to, out, total_tokens, Hq, 32)) != TSK_OK) return st;
 
   char name[96];
   snprintf(name, sizeof name, "tsk_mha_prefill[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,T=%lld]", Hq, Hkv,
@@ -282,7 +289,10 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
   p.debug_stall = g_debug_stall;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  tsk::attention_fwd_kernel<<<grid, tsk::kThreads, tsk::kSmemBytes, stream>>>(tq, tk, tv, p);
+  if (window > 0 && window <= tsk::kSmallWindowMax)
+    tsk::attention_fwd_kernel<true><<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(tq, tk, tv, to, p);
+  else
+    tsk::attention_fwd_kernel<false><<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(tq, tk, tv, to, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) note_error("attention kernel launch", e);
   if (prof) {
@@ -430,10 +440,11 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
     scratch = static_cast<int*>(ptr);
   }
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((st = encode_thd(&tq, q, total_tokens, Hq)) != TSK_OK) return st;
   if ((st = encode_thd(&tk, k, total_tokens, Hkv)) != TSK_OK) return st;
   if ((st = encode_thd(&tv, v, total_tokens, Hkv)) != TSK_OK) return st;
+  if ((st = encode_thd(&to, out, total_tokens, Hq, 32)) != TSK_OK) return st;
 
   int* tile_off = scratch + tsk::kWsHeader;
   int4* list = reinterpret_cast<int4*>(scratch + kNoAllocOffInts);
@@ -462,7 +473,10 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   p.debug_stall = 0;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  tsk::attention_fwd_kernel<<<grid, tsk::kThreads, tsk::kSmemBytes, stream>>>(tq, tk, tv, p);
+  if (window > 0 && window <= tsk::kSmallWindowMax)
+    tsk::attention_fwd_kernel<true><<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(tq, tk, tv, to, p);
+  else
+    tsk::attention_fwd_kernel<false><<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(tq, tk, tv, to, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     note_error("attention kernel launch (no-alloc)", e);

@@ -134,7 +134,9 @@ TSK_API tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall);
  * n counters into `out`: out[i] = clock cycles spent at code site i, summed
  * over lane 0 of every warp that passed it, and out[64 + i] = the number of
  * passes; then clears them.  Sites 1..15 are the bounded waits (numbered as
- * the status word reports them), 20..23 softmax phases, 30 softmax total.
+ * the status word reports them), 20..28 softmax phases, 30 softmax total.
+ * out[128 + b] (b < 1024) is the run time in ns of block b in the last
+ * launch.
  */
 TSK_API tsk_status tsk_debug_trace(unsigned long long *out, int32_t n);
 
