@@ -114,6 +114,10 @@ class Workload:
     sinks: np.ndarray | None  # float32 [Hq] or None
     cu_seqlens: np.ndarray   # int32 [S+1]
     seed: int
+    # prefill over a key/value cache: keys/values per sequence (Lk >= Lq), the
+    # new tokens' keys last; None for plain prefill (keys == queries)
+    cu_seqlens_k: np.ndarray | None = None
+    seqlens_k: list | None = None
 
     @property
     def total_tokens(self) -> int:
@@ -123,15 +127,20 @@ class Workload:
     def num_seqs(self) -> int:
         return len(self.seqlens)
 
+    @property
+    def total_keys(self) -> int:
+        return int(self.cu_seqlens_k[-1]) if self.cu_seqlens_k is not None else self.total_tokens
+
     def allowed_keys(self) -> int:
-        """Sum over (token) rows of the number of allowed keys, for one head."""
+        """Sum over query rows of the number of allowed keys, for one head."""
         tot = 0
-        for L in self.seqlens:
-            t = np.arange(L, dtype=np.int64)
+        lks = self.seqlens_k if self.seqlens_k is not None else self.seqlens
+        for L, Lk in zip(self.seqlens, lks):
+            pos = np.arange(L, dtype=np.int64) + (Lk - L)   # key position of each query
             if self.window > 0:
-                tot += int(np.minimum(t + 1, self.window).sum())
+                tot += int(np.minimum(pos + 1, self.window).sum())
             else:
-                tot += int((t + 1).sum())
+                tot += int((pos + 1).sum())
         return tot
 
     def unmasked_flops(self) -> float:
@@ -140,8 +149,8 @@ class Workload:
 
     def algorithmic_bytes(self) -> int:
         """Read Q, K, V once; write out (bf16) and lse (fp32) once."""
-        T = self.total_tokens
-        return T * (2 * self.Hq * self.D * 2 + 2 * self.Hkv * self.D * 2 + 4 * self.Hq)
+        T, Tk = self.total_tokens, self.total_keys
+        return T * (2 * self.Hq * self.D * 2 + 4 * self.Hq) + Tk * 2 * self.Hkv * self.D * 2
 
 
 def make(seqlens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, sink_sigma=1.0,
@@ -158,6 +167,27 @@ def make(seqlens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, sink_sigma=1.0,
     return Workload(name, seqlens, Hq, Hkv, D, window, scale, q, k, v, sinks, cu, seed)
 
 
+def make_kvcache(q_lens, k_lens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, sink_sigma=1.0,
+                 with_sinks=True, name="kvcache") -> Workload:
+    """Prefill over a cache: sequence s has q_lens[s] new tokens and k_lens[s]
+    >= q_lens[s] keys/values (cached prefix, then the new tokens' own)."""
+    q_lens = [int(x) for x in q_lens]
+    k_lens = [int(x) for x in k_lens]
+    assert len(q_lens) == len(k_lens) and all(k >= q for q, k in zip(q_lens, k_lens))
+    cu = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    cu_k = np.zeros(len(k_lens) + 1, dtype=np.int32)
+    if q_lens:
+        cu[1:] = np.cumsum(np.asarray(q_lens, dtype=np.int64)).astype(np.int32)
+        cu_k[1:] = np.cumsum(np.asarray(k_lens, dtype=np.int64)).astype(np.int32)
+    T, Tk = int(cu[-1]), int(cu_k[-1])
+    q = normal_bf16(seed, STREAM_Q, (T, Hq, D))
+    k = normal_bf16(seed, STREAM_K, (Tk, Hkv, D))
+    v = normal_bf16(seed, STREAM_V, (Tk, Hkv, D))
+    sinks = normal_f32(seed, STREAM_SINKS, (Hq,), sink_sigma) if with_sinks else None
+    return Workload(name, q_lens, Hq, Hkv, D, window, scale, q, k, v, sinks, cu, seed,
+                    cu_seqlens_k=cu_k, seqlens_k=k_lens)
+
+
 # The five configurations, smallest first.
 CONFIGS = {
     "tiny_1x256_h4kv1": dict(desc="1 seq x 256 tokens, Hq=4, Hkv=1, D=64, sinks N(0,1), "
@@ -170,6 +200,9 @@ CONFIGS = {
     "ragged32_w128_h64kv8": dict(desc="ragged32 rerun with W=128"),
     "long_1x32768_h64kv8": dict(desc="1 seq x 32768 tokens, K = bf16(3*N(0,1)), sinks N(0,1), "
                                      "full causal"),
+    # prefill over a key/value cache (not one of the five above)
+    "kvcache_4x2048_on_4096_h64kv8": dict(desc="4 seqs x 2048 new tokens over a 4096-token cache "
+                                               "(Lk = 6144), Hq=64, Hkv=8, D=64, causal"),
 }
 
 
@@ -190,6 +223,8 @@ def config(name: str, seed: int = 0) -> Workload:
         return make(ragged_lengths(seed), 64, 8, window=128, sink_sigma=2.0, seed=seed, name=name)
     if name == "long_1x32768_h64kv8":
         return make([32768], 64, 8, k_mult=3.0, seed=seed, name=name)
+    if name == "kvcache_4x2048_on_4096_h64kv8":
+        return make_kvcache([2048] * 4, [6144] * 4, 64, 8, seed=seed, name=name)
     raise KeyError(name)
 
 

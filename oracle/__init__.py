@@ -54,6 +54,15 @@ def _bind(lib):
                                             ctypes.c_double, P, P, ctypes.c_int64, P, P,
                                             ctypes.c_int]
     lib.oracle_mha_prefill_rows.restype = ctypes.c_int
+    lib.oracle_mha_prefill_kvcache.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double, P, P, ctypes.c_int]
+    lib.oracle_mha_prefill_kvcache.restype = ctypes.c_int
+    lib.oracle_mha_prefill_kvcache_rows.argtypes = [P, P, P, P, P, P, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_double, P, P,
+                                                    ctypes.c_int64, P, P, ctypes.c_int]
+    lib.oracle_mha_prefill_kvcache_rows.restype = ctypes.c_int
     return lib
 
 
@@ -115,9 +124,41 @@ def mha_prefill_rows(q, k, v, sinks, cu_seqlens, Hq, Hkv, D, window, scale, row_
     return out, lse, n
 
 
+def mha_prefill_kvcache(q, k, v, sinks, cu_q, cu_k, Hq, Hkv, D, window, scale, rows=None,
+                        nthreads=0, lib=None):
+    """Prefill over a key/value cache (query i of a sequence at key position
+    Lk - Lq + i).  Returns (out, lse, threads) for every row, or for the rows
+    (t, h) given."""
+    lib = lib or _load()
+    q, k, v, s, cu_q = _prep(q, k, v, sinks, cu_q)
+    cu_k = np.ascontiguousarray(cu_k, dtype=np.int32)
+    if rows is None:
+        Tq = int(cu_q[-1])
+        out = np.zeros((Tq, Hq, D), dtype=np.float64)
+        lse = np.zeros((Tq, Hq), dtype=np.float64)
+        n = lib.oracle_mha_prefill_kvcache(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(cu_q),
+                                           _ptr(cu_k), len(cu_q) - 1, Hq, Hkv, D, window,
+                                           float(scale), _ptr(out), _ptr(lse), nthreads)
+    else:
+        row_t = np.ascontiguousarray(rows[0], dtype=np.int64)
+        row_h = np.ascontiguousarray(rows[1], dtype=np.int32)
+        out = np.zeros((len(row_t), D), dtype=np.float64)
+        lse = np.zeros(len(row_t), dtype=np.float64)
+        n = lib.oracle_mha_prefill_kvcache_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(cu_q),
+                                                _ptr(cu_k), len(cu_q) - 1, Hq, Hkv, D, window,
+                                                float(scale), _ptr(row_t), _ptr(row_h),
+                                                len(row_t), _ptr(out), _ptr(lse), nthreads)
+    if n < 0:
+        raise ValueError(f"oracle rejected the problem (rc={n})")
+    return out, lse, n
+
+
 def run_workload(w, rows=None, nthreads=0):
     """Convenience over an inputgen.Workload (full, or sampled rows (t, h))."""
     sinks = None if w.sinks is None else w.sinks.astype(np.float64)
+    if getattr(w, "cu_seqlens_k", None) is not None:
+        return mha_prefill_kvcache(w.q, w.k, w.v, sinks, w.cu_seqlens, w.cu_seqlens_k, w.Hq,
+                                   w.Hkv, w.D, w.window, w.scale, rows=rows, nthreads=nthreads)
     if rows is None:
         return mha_prefill(w.q, w.k, w.v, sinks, w.cu_seqlens, w.Hq, w.Hkv, w.D, w.window,
                            w.scale, nthreads)

@@ -25,6 +25,14 @@
  * are bf16 bit patterns widened exactly to double; every sum is in double.
  * Each row is evaluated in the two-pass form (max, then exponentials).
  *
+ * Prefill over a key/value cache (the README's `mha_prefill_with_kvcache`
+ * call, section "Public API"; the pages give no formula): sequence s has Lq
+ * new query tokens (rows cu_q[s].. of q) and Lk >= Lq keys (rows cu_k[s].. of
+ * k and v: the cached prefix followed by the new tokens' keys).  New token i
+ * sits at key position P = Lk - Lq + i and attends to key positions
+ * max(0, P-W+1) .. P (causal aligned to the end of the keys).  With Lk == Lq
+ * this is the prefill above.
+ *
  * Plain C99 + pthreads; portable (no architecture-specific code).
  */
 #include <math.h>
@@ -37,9 +45,10 @@
 typedef struct {
   const uint16_t *q, *k, *v;
   const double *sinks;
-  const int32_t *cu;
+  const int32_t *cu;   /* query sequence offsets */
   int num_seqs, Hq, Hkv, D, window;
   double scale;
+  const int32_t *cu_k; /* key sequence offsets (== cu for plain prefill) */
 } problem_t;
 
 static double bf16_to_double(uint16_t b) {
@@ -49,16 +58,18 @@ static double bf16_to_double(uint16_t b) {
   return (double)f;
 }
 
-/* One output row: token t (absolute index) of a sequence starting at `start`,
- * query head h.  `work` holds at least t-start+1 doubles. */
-static void one_row(const problem_t *p, int64_t start, int64_t t, int h, double *out_row,
-                    double *lse_out, double *work, double *qrow) {
+/* One output row: query row tq (absolute), query head h; the query sits at
+ * absolute key row t of a key sequence starting at start_k.  `work` holds at
+ * least t-start_k+1 doubles. */
+static void one_row(const problem_t *p, int64_t tq, int64_t start_k, int64_t t, int h,
+                    double *out_row, double *lse_out, double *work, double *qrow) {
+  /* tq: absolute query row; t: absolute key row of the query's own position */
   const int D = p->D, G = p->Hq / p->Hkv, g = h / G;
-  int64_t lo = start;
+  int64_t lo = start_k;
   if (p->window > 0 && t - p->window + 1 > lo) lo = t - p->window + 1;
   const int64_t n = t - lo + 1;
 
-  for (int d = 0; d < D; ++d) qrow[d] = bf16_to_double(p->q[(t * p->Hq + h) * (int64_t)D + d]);
+  for (int d = 0; d < D; ++d) qrow[d] = bf16_to_double(p->q[(tq * p->Hq + h) * (int64_t)D + d]);
 
   /* pass 1: scores and their maximum (sink included) */
   double M = -INFINITY;
@@ -156,7 +167,10 @@ static void *worker(void *arg) {
         lrow = sh->lse ? sh->lse + i : 0;
       }
       int64_t s = seq_of_token(p, t);
-      one_row(p, p->cu[s], t, h, orow, lrow, work, qrow);
+      const int64_t lq = (int64_t)p->cu[s + 1] - p->cu[s];
+      const int64_t lk = (int64_t)p->cu_k[s + 1] - p->cu_k[s];
+      const int64_t pos = p->cu_k[s] + (lk - lq) + (t - p->cu[s]);
+      one_row(p, t, p->cu_k[s], pos, h, orow, lrow, work, qrow);
     }
   }
   free(work);
@@ -165,12 +179,14 @@ static void *worker(void *arg) {
 }
 
 static int check_problem(const problem_t *p) {
-  if (!p->q || !p->k || !p->v || !p->cu) return -1;
+  if (!p->q || !p->k || !p->v || !p->cu || !p->cu_k) return -1;
   if (p->num_seqs < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0) return -1;
   if (p->Hq % p->Hkv) return -1;
-  if (p->cu[0] != 0) return -1;
-  for (int s = 0; s < p->num_seqs; ++s)
-    if (p->cu[s + 1] < p->cu[s]) return -1;
+  if (p->cu[0] != 0 || p->cu_k[0] != 0) return -1;
+  for (int s = 0; s < p->num_seqs; ++s) {
+    if (p->cu[s + 1] < p->cu[s] || p->cu_k[s + 1] < p->cu_k[s]) return -1;
+    if (p->cu_k[s + 1] - p->cu_k[s] < p->cu[s + 1] - p->cu[s]) return -1; /* Lk >= Lq */
+  }
   return 0;
 }
 
@@ -178,7 +194,7 @@ static int run(shared_t *sh, int nthreads) {
   const problem_t *p = sh->p;
   int64_t max_len = 1;
   for (int s = 0; s < p->num_seqs; ++s) {
-    int64_t L = (int64_t)p->cu[s + 1] - p->cu[s];
+    int64_t L = (int64_t)p->cu_k[s + 1] - p->cu_k[s];
     if (L > max_len) max_len = L;
   }
   sh->max_len = max_len;
@@ -198,6 +214,39 @@ static int run(shared_t *sh, int nthreads) {
   return sh->err ? -2 : started + 1;
 }
 
+static int run_full(const problem_t *p, double *out, double *lse, int nthreads) {
+  if (check_problem(p) || !out) return -1;
+  pthread_mutex_t mu = PTHREAD_MUTEX_INITIALIZER;
+  shared_t sh;
+  memset(&sh, 0, sizeof sh);
+  sh.p = p;
+  sh.out = out;
+  sh.lse = lse;
+  sh.mode = 0;
+  sh.mu = &mu;
+  return run(&sh, nthreads);
+}
+
+static int run_rows(const problem_t *p, const int64_t *row_t, const int32_t *row_h,
+                    int64_t nrows, double *out, double *lse, int nthreads) {
+  if (check_problem(p) || !out || (nrows > 0 && (!row_t || !row_h))) return -1;
+  const int64_t T = p->cu[p->num_seqs];
+  for (int64_t i = 0; i < nrows; ++i)
+    if (row_t[i] < 0 || row_t[i] >= T || row_h[i] < 0 || row_h[i] >= p->Hq) return -1;
+  pthread_mutex_t mu = PTHREAD_MUTEX_INITIALIZER;
+  shared_t sh;
+  memset(&sh, 0, sizeof sh);
+  sh.p = p;
+  sh.out = out;
+  sh.lse = lse;
+  sh.row_t = row_t;
+  sh.row_h = row_h;
+  sh.nrows = nrows;
+  sh.mode = 1;
+  sh.mu = &mu;
+  return run(&sh, nthreads);
+}
+
 /*
  * Full evaluation.  q: [T,Hq,D], k/v: [T,Hkv,D] bf16 bits; sinks: [Hq] or NULL;
  * cu_seqlens: [num_seqs+1]; out: [T,Hq,D] double; lse: [T,Hq] double or NULL.
@@ -207,17 +256,8 @@ int oracle_mha_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        const double *sinks, const int32_t *cu_seqlens, int num_seqs, int Hq,
                        int Hkv, int D, int window, double scale, double *out, double *lse,
                        int nthreads) {
-  problem_t p = {q, k, v, sinks, cu_seqlens, num_seqs, Hq, Hkv, D, window, scale};
-  if (check_problem(&p) || !out) return -1;
-  pthread_mutex_t mu = PTHREAD_MUTEX_INITIALIZER;
-  shared_t sh;
-  memset(&sh, 0, sizeof sh);
-  sh.p = &p;
-  sh.out = out;
-  sh.lse = lse;
-  sh.mode = 0;
-  sh.mu = &mu;
-  return run(&sh, nthreads);
+  problem_t p = {q, k, v, sinks, cu_seqlens, num_seqs, Hq, Hkv, D, window, scale, cu_seqlens};
+  return run_full(&p, out, lse, nthreads);
 }
 
 /*
@@ -229,21 +269,28 @@ int oracle_mha_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t
                             int Hq, int Hkv, int D, int window, double scale,
                             const int64_t *row_t, const int32_t *row_h, int64_t nrows,
                             double *out, double *lse, int nthreads) {
-  problem_t p = {q, k, v, sinks, cu_seqlens, num_seqs, Hq, Hkv, D, window, scale};
-  if (check_problem(&p) || !out || (nrows > 0 && (!row_t || !row_h))) return -1;
-  const int64_t T = cu_seqlens[num_seqs];
-  for (int64_t i = 0; i < nrows; ++i)
-    if (row_t[i] < 0 || row_t[i] >= T || row_h[i] < 0 || row_h[i] >= Hq) return -1;
-  pthread_mutex_t mu = PTHREAD_MUTEX_INITIALIZER;
-  shared_t sh;
-  memset(&sh, 0, sizeof sh);
-  sh.p = &p;
-  sh.out = out;
-  sh.lse = lse;
-  sh.row_t = row_t;
-  sh.row_h = row_h;
-  sh.nrows = nrows;
-  sh.mode = 1;
-  sh.mu = &mu;
-  return run(&sh, nthreads);
+  problem_t p = {q, k, v, sinks, cu_seqlens, num_seqs, Hq, Hkv, D, window, scale, cu_seqlens};
+  return run_rows(&p, row_t, row_h, nrows, out, lse, nthreads);
+}
+
+/*
+ * Prefill over a key/value cache.  q: [Tq,Hq,D] with cu_q; k/v: [Tk,Hkv,D] with
+ * cu_k (per sequence Lk >= Lq); out: [Tq,Hq,D]; lse: [Tq,Hq] or NULL.
+ */
+int oracle_mha_prefill_kvcache(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const double *sinks, const int32_t *cu_q, const int32_t *cu_k,
+                               int num_seqs, int Hq, int Hkv, int D, int window, double scale,
+                               double *out, double *lse, int nthreads) {
+  problem_t p = {q, k, v, sinks, cu_q, num_seqs, Hq, Hkv, D, window, scale, cu_k};
+  return run_full(&p, out, lse, nthreads);
+}
+
+int oracle_mha_prefill_kvcache_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                    const double *sinks, const int32_t *cu_q,
+                                    const int32_t *cu_k, int num_seqs, int Hq, int Hkv, int D,
+                                    int window, double scale, const int64_t *row_t,
+                                    const int32_t *row_h, int64_t nrows, double *out,
+                                    double *lse, int nthreads) {
+  problem_t p = {q, k, v, sinks, cu_q, num_seqs, Hq, Hkv, D, window, scale, cu_k};
+  return run_rows(&p, row_t, row_h, nrows, out, lse, nthreads);
 }

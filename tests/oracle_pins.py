@@ -19,6 +19,13 @@ Pins:
   * perm    -- permuting the packed sequences permutes the rows exactly;
   * gqa     -- GQA equals MHA with K/V repeated per group, exactly;
   * rows    -- the sampled-row entry point equals the full one at those rows.
+
+Prefill over a key/value cache:
+  * kv_equal   -- Lk == Lq is exactly plain prefill;
+  * kv_chunked -- the last Lq tokens of a full prefill equal a prefill of
+                  those tokens over the whole sequence's keys, exactly;
+  * kv_sdpa    -- library softmax attention with the causal rule aligned to
+                  the end of the keys (query i at key position Lk - Lq + i).
 """
 from __future__ import annotations
 
@@ -314,3 +321,89 @@ def run_all(lib):
         except Exception as e:  # a mutant may also crash a pin
             res[name] = (False, f"raised {type(e).__name__}: {e}")
     return res
+
+
+# --------------------------------------------------------------------------- prefill over a cache
+def _kv_case(seed, q_lens, k_lens, window=0, Hq=4, Hkv=2, D=16, sinks=True, scale=0.25):
+    return inputgen.make_kvcache(q_lens, k_lens, Hq, Hkv, D=D, window=window, scale=scale,
+                                 seed=seed, with_sinks=sinks)
+
+
+def _kv_run(lib, w, rows=None):
+    s = None if w.sinks is None else w.sinks.astype(np.float64)
+    out, lse, _ = oracle.mha_prefill_kvcache(w.q, w.k, w.v, s, w.cu_seqlens, w.cu_seqlens_k,
+                                             w.Hq, w.Hkv, w.D, w.window, w.scale, rows=rows,
+                                             nthreads=2, lib=lib)
+    return out, lse
+
+
+def pin_kv_equal_lengths(lib):
+    """Lk == Lq is plain prefill, exactly."""
+    w = _kv_case(31, [5, 17, 40], [5, 17, 40], window=6)
+    o1, l1 = _kv_run(lib, w)
+    o2, l2 = _run(lib, w)
+    return np.array_equal(o1, o2) and np.array_equal(l1, l2), "kvcache(Lk=Lq) vs prefill"
+
+
+def pin_kv_chunked_prefill(lib):
+    """The last Lq tokens of a full prefill equal a prefill of those tokens
+    over a cache holding the whole sequence's keys/values."""
+    ok = True
+    for window in (0, 5):
+        full = small_workload(seed=32, seqlens=(9, 30, 41), window=window)
+        o_full, l_full = _run(lib, full)
+        q_lens = [3, 30, 7]
+        idx = np.concatenate([np.arange(full.cu_seqlens[s + 1] - q, full.cu_seqlens[s + 1])
+                              for s, q in enumerate(q_lens)])
+        cu_q = np.zeros(4, np.int32)
+        cu_q[1:] = np.cumsum(q_lens)
+        s = full.sinks.astype(np.float64)
+        o, l, _ = oracle.mha_prefill_kvcache(full.q[idx], full.k, full.v, s, cu_q,
+                                             full.cu_seqlens, full.Hq, full.Hkv, full.D, window,
+                                             full.scale, nthreads=2, lib=lib)
+        ok &= np.array_equal(o, o_full[idx]) and np.array_equal(l, l_full[idx])
+    return ok, "chunked prefill vs full prefill"
+
+
+def sdpa_kvcache_reference(w):
+    G = w.Hq // w.Hkv
+    out = np.zeros((w.total_tokens, w.Hq, w.D))
+    lse = np.zeros((w.total_tokens, w.Hq))
+    qf, kf, vf = (torch.from_numpy(_f64(x)) for x in (w.q, w.k, w.v))
+    for si, (Lq, Lk) in enumerate(zip(w.seqlens, w.seqlens_k)):
+        if Lq == 0:
+            continue
+        sq, sk = int(w.cu_seqlens[si]), int(w.cu_seqlens_k[si])
+        q = qf[sq:sq + Lq].permute(1, 0, 2)
+        k = kf[sk:sk + Lk].repeat_interleave(G, dim=1).permute(1, 0, 2)
+        v = vf[sk:sk + Lk].repeat_interleave(G, dim=1).permute(1, 0, 2)
+        zero = torch.zeros(w.Hq, 1, w.D, dtype=torch.float64)
+        kk, vv = torch.cat([k, zero], 1), torch.cat([v, zero], 1)
+        pos = torch.arange(Lq)[:, None] + (Lk - Lq)
+        ji = torch.arange(Lk)[None, :]
+        allowed = ji <= pos
+        if w.window > 0:
+            allowed &= ji >= pos - w.window + 1
+        m = torch.zeros(Lq, Lk, dtype=torch.float64).masked_fill(~allowed, float("-inf"))
+        sink_col = torch.from_numpy(np.asarray(w.sinks, np.float64)).view(w.Hq, 1, 1).expand(w.Hq, Lq, 1)
+        mask = torch.cat([m.expand(w.Hq, Lq, Lk), sink_col], 2)
+        o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask, scale=w.scale)
+        lg = torch.logsumexp(w.scale * (q @ kk.transpose(1, 2)) + mask, dim=-1)
+        out[sq:sq + Lq] = o.permute(1, 0, 2).numpy()
+        lse[sq:sq + Lq] = lg.permute(1, 0).numpy()
+    return out, lse
+
+
+def pin_kv_sdpa(lib):
+    worst = 0.0
+    for seed, ql, kl, window in [(33, [1, 4, 20], [9, 4, 50], 0), (34, [3, 16], [40, 17], 6),
+                                 (35, [7], [7], 0), (36, [2, 1, 33], [2, 30, 33], 1)]:
+        w = _kv_case(seed, ql, kl, window=window)
+        o, l = _kv_run(lib, w)
+        ro, rl = sdpa_kvcache_reference(w)
+        worst = max(worst, np.abs(o - ro).max(), np.abs(l - rl).max())
+    return worst < 1e-10, f"max err {worst:.3g}"
+
+
+ALL_PINS.update({"kv_equal": pin_kv_equal_lengths, "kv_chunked": pin_kv_chunked_prefill,
+                 "kv_sdpa": pin_kv_sdpa})

@@ -30,6 +30,7 @@ MUTANTS = {
     "value_reads_keys": ("const uint16_t *vr = p->v +", "const uint16_t *vr = p->k +"),
     "scale_missing": ("work[j] = p->scale * acc;", "work[j] = acc;"),
     "no_causal_bound_max_missing_sink": ("if (has_sink && sink > M) M = sink;", ""),
+    "kvcache_top_left_alignment": ("p->cu_k[s] + (lk - lq) + (t - p->cu[s])", "p->cu_k[s] + (t - p->cu[s])"),
 }
 
 
