@@ -154,6 +154,8 @@ def oracle_rate(w, seconds_target, seed_stream=77):
         h = (r % w.Hq).astype(np.int32)
         s = np.searchsorted(cu, t, side="right") - 1
         pos = t - cu[s]
+        if w.cu_seqlens_k is not None:   # key position of the query (cache prefix first)
+            pos = pos + (np.diff(w.cu_seqlens_k)[s] - np.diff(cu)[s])
         nk = pos + 1 if w.window <= 0 else np.minimum(pos + 1, w.window)
         return t, h, float(4.0 * w.D * nk.sum())
 
@@ -215,7 +217,8 @@ def run_reference(args, ws, rank):
         "ms_per_step": ms_equiv, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
-                   f"{len(w.seqlens)} seqs", "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   f"{len(w.seqlens)} seqs", "key_lengths": w.seqlens_k,
+                   "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "window": w.window, "note": "ms_per_step extrapolated from the sampled rate"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                          "sample": f"{rows} uniform (token, head) rows per step of {w.name}, "
@@ -272,15 +275,21 @@ def main():
     h_v = torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).pin_memory()
     h_s = torch.from_numpy(w.sinks).pin_memory()
     h_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
+    kvcache = w.cu_seqlens_k is not None
+    h_cuk = torch.from_numpy(w.cu_seqlens_k if kvcache else w.cu_seqlens).pin_memory()
     q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
-    sinks, cu = h_s.to(dev), h_cu.to(dev)
+    sinks, cu, cuk = h_s.to(dev), h_cu.to(dev), h_cuk.to(dev)
     out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
-    def step(o=out, l=lse, qq=q, kk=k, vv=v, ss=sinks, cc=cu):
-        rc = pkg.tsk_mha_prefill(qq, kk, vv, ss, cc, w.num_seqs, T, Hq, Hkv, D, w.window,
-                                 w.scale, o, l, stream)
+    def step(o=out, l=lse, qq=q, kk=k, vv=v, ss=sinks, cc=cu, ck=cuk):
+        if kvcache:
+            rc = pkg.tsk_mha_prefill_kvcache(qq, kk, vv, ss, cc, ck, w.num_seqs, T, w.total_keys,
+                                             Hq, Hkv, D, w.window, w.scale, o, l, stream)
+        else:
+            rc = pkg.tsk_mha_prefill(qq, kk, vv, ss, cc, w.num_seqs, T, Hq, Hkv, D, w.window,
+                                     w.scale, o, l, stream)
         if rc != 0:
             raise pkg.TskError(rc, "tsk_mha_prefill")
 
@@ -323,7 +332,7 @@ def main():
     h_out = torch.empty((T, Hq, D), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((T, Hq), dtype=torch.float32).pin_memory()
     d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    d_s, d_cu = torch.empty_like(sinks), torch.empty_like(cu)
+    d_s, d_cu, d_cuk = torch.empty_like(sinks), torch.empty_like(cu), torch.empty_like(cuk)
     pkg.tsk_profile_enable(False)
 
     def e2e_step():
@@ -332,7 +341,9 @@ def main():
         d_v.copy_(h_v, non_blocking=True)
         d_s.copy_(h_s, non_blocking=True)
         d_cu.copy_(h_cu, non_blocking=True)
-        step(out, lse, d_q, d_k, d_v, d_s, d_cu)
+        if kvcache:
+            d_cuk.copy_(h_cuk, non_blocking=True)
+        step(out, lse, d_q, d_k, d_v, d_s, d_cu, d_cuk if kvcache else d_cu)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -349,7 +360,8 @@ def main():
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
     e2e_ms = reduce_max(sum(e_ms) / len(e_ms), ws)
-    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_s, h_cu))
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_s, h_cu)) + \
+        (h_cuk.numel() * 4 if kvcache else 0)
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
     # the e2e outputs must equal the resident-input outputs
     torch.cuda.synchronize()
@@ -369,7 +381,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, fp32 sinks)",
         "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
-                   f"{len(w.seqlens)} seqs", "total_tokens": T, "Hq": Hq, "Hkv": Hkv, "D": D,
+                   f"{len(w.seqlens)} seqs", "total_tokens": T,
+                   "key_lengths": (w.seqlens_k if kvcache else None), "Hq": Hq, "Hkv": Hkv, "D": D,
                    "window": w.window, "scale": w.scale, "sinks": True, "lse": True,
                    "l2": "flushed before every timed step (256 MB write)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},

@@ -19,7 +19,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "mha_prefill", "tsk_get_device_status", "tsk_status_string",
+__all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "tsk_mha_prefill_kvcache",
+           "mha_prefill", "mha_prefill_kvcache", "tsk_get_device_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
            "tsk_version", "TskError", "library_path", "load_library"]
@@ -73,6 +74,9 @@ def load_library():
         lib.tsk_mha_prefill.restype = ctypes.c_int
         lib.tsk_mha_prefill_noalloc.argtypes = lib.tsk_mha_prefill.argtypes
         lib.tsk_mha_prefill_noalloc.restype = ctypes.c_int
+        lib.tsk_mha_prefill_kvcache.argtypes = [P, P, P, P, P, P, i32, i64, i64, i32, i32, i32,
+                                                i32, ctypes.c_float, P, P, P]
+        lib.tsk_mha_prefill_kvcache.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
         lib.tsk_last_error.argtypes = []
@@ -144,6 +148,51 @@ def tsk_mha_prefill_noalloc(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, 
                                        int(num_seqs), int(total_tokens), int(Hq), int(Hkv),
                                        int(D), int(window), float(scale), _ptr(out), _ptr(lse),
                                        _stream_handle(stream))
+
+
+def tsk_mha_prefill_kvcache(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
+                            total_k, Hq, Hkv, D, window, scale, out, lse, stream=None) -> int:
+    """Prefill over a key/value cache (same arguments as the C function): new
+    token i of a sequence with Lq new tokens and Lk keys sits at key position
+    Lk - Lq + i.  Returns the status code."""
+    lib = load_library()
+    return lib.tsk_mha_prefill_kvcache(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks),
+                                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(num_seqs),
+                                       int(total_q), int(total_k), int(Hq), int(Hkv), int(D),
+                                       int(window), float(scale), _ptr(out), _ptr(lse),
+                                       _stream_handle(stream))
+
+
+def mha_prefill_kvcache(q, k, v, cu_seqlens_q, cu_seqlens_k, sinks=None, window: int = 0,
+                        scale: float | None = None, out=None, lse=None, return_lse=True,
+                        stream=None):
+    """Tensor-level convenience over ``tsk_mha_prefill_kvcache``: q [Tq, Hq, 64],
+    k/v [Tk, Hkv, 64] bf16 CUDA, int32 CUDA offsets.  Returns (out, lse)."""
+    import torch
+    Tq, Hq, D = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if v.shape != k.shape or k.shape[2] != D:
+        raise ValueError("k and v must both be [Tk, Hkv, D]")
+    for name, c in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if c.dtype != torch.int32 or not c.is_cuda:
+            raise ValueError(f"{name} must be an int32 CUDA tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    rc = tsk_mha_prefill_kvcache(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k,
+                                 cu_seqlens_q.numel() - 1, Tq, Tk, Hq, Hkv, D, window, scale, out,
+                                 lse if return_lse else None, stream)
+    if rc != 0:
+        raise TskError(rc, "tsk_mha_prefill_kvcache")
+    return out, (lse if return_lse else None)
 
 
 def mha_prefill(q, k, v, cu_seqlens, sinks=None, window: int = 0, scale: float | None = None,

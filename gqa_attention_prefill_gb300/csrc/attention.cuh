@@ -68,7 +68,7 @@ struct AttnParams {
   const float* sinks;   // [Hq] or nullptr
   __nv_bfloat16* out;   // [T, Hq, 64]
   float* lse;           // [T, Hq] or nullptr
-  const int4* list;     // sorted query tiles (QTile)
+  const int4* list;     // sorted query tiles (two int4 per tile, see schedule.cuh)
   const int* ws;        // ws[kWsNTiles] = number of query tiles
   int* status;          // device status words
   int Hq, Hkv, G, HP;   // HP = ceil(G / 2) head pairs per KV head
@@ -106,19 +106,24 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, in
 
 struct Unit {
   int start, q0, kv_lo, len, n_kv, g, h0, ntiles;
+  int start_k;  // first key row of the sequence
+  int offset;   // Lk - Lq: key position of query row 0
 };
 
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   const int per_tile = p.Hkv * p.HP;
   const int qi = u / per_tile;
   const int rem = u - qi * per_tile;
-  const int4 e = __ldg(p.list + qi);
+  const int4 e = __ldg(p.list + 2 * qi);
+  const int4 f = __ldg(p.list + 2 * qi + 1);
   Unit r;
   r.start = e.x;
   r.q0 = e.y;
   r.kv_lo = e.z;
   r.len = e.w;
-  r.n_kv = e.y / kTileM - e.z + 1;
+  r.start_k = f.x;
+  r.offset = f.y;
+  r.n_kv = f.z;
   r.g = rem / p.HP;
   const int hp = rem - r.g * p.HP;
   r.h0 = r.g * p.G + 2 * hp;
@@ -160,7 +165,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
       const uint32_t k = kv_iter / kStages;
       if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, 2, p, cx.abort);
       if (!ok) break;
-      const int row = w.start + (w.kv_lo + j) * kTileN;
+      const int row = w.start_k + (w.kv_lo + j) * kTileN;
       const uint32_t kdst = cx.sbase + kSmemKV + s * 2 * kTileBytes;
       mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTileBytes);
       tma_load_3d(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, row);
@@ -264,11 +269,11 @@ struct ChunkMask {
   uint32_t partial;  // bit k: chunk k needs a per-element test
 };
 
-// Allowed keys of query row `row` (relative to the sequence start) in the key
-// tile starting at `kbase`: columns c with lo_c <= c <= hi_c, where
-// hi_c = row - kbase and lo_c = row - window + 1 - kbase (window > 0).  The
-// warp's rows are row0 .. row0 + 31, so the bounds of its lanes 0 and 31
-// decide each chunk uniformly.
+// Allowed keys of a query at key position `pos` (relative to the sequence's
+// first key) in the key tile starting at `kbase`: columns c with lo_c <= c <=
+// hi_c, where hi_c = pos - kbase and lo_c = pos - window + 1 - kbase
+// (window > 0).  The warp's queries sit at row0 .. row0 + 31, so the bounds
+// of its lanes 0 and 31 decide each chunk uniformly.
 __device__ __forceinline__ ChunkMask classify_chunks(int row0, int kbase, int window) {
   ChunkMask m{0u, 0u};
   const int hi_min = row0 - kbase, hi_max = hi_min + 31;
@@ -305,7 +310,8 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     const Unit w = decode_unit(p, u);
     if (t >= w.ntiles) continue;
     const int h = w.h0 + t;
-    const int row = w.q0 + r;  // relative to sequence start
+    const int row = w.q0 + r;        // query row, relative to the sequence's first query
+    const int pos = w.offset + row;  // its key position
     float m_used = -INFINITY, l = 0.f;
     if (p.sinks) {
       m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
@@ -333,11 +339,11 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       const int kbase = kt * kTileN;
-      const bool edge = (kbase + kTileN - 1 > w.q0) ||
-                        (p.window > 0 && kbase < w.q0 + kTileM - p.window);
+      const bool edge = (kbase + kTileN - 1 > w.offset + w.q0) ||
+                        (p.window > 0 && kbase < w.offset + w.q0 + kTileM - p.window);
       if (edge) {
-        const int hi_c = row - kbase;
-        const int lo_c = p.window > 0 ? row - p.window + 1 - kbase : -1;
+        const int hi_c = pos - kbase;
+        const int lo_c = p.window > 0 ? pos - p.window + 1 - kbase : -1;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > hi_c || c < lo_c) s[c] = -INFINITY;
@@ -469,7 +475,8 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     const Unit w = decode_unit(p, u);
     if (t >= w.ntiles) continue;
     const int h = w.h0 + t;
-    const int row = w.q0 + r;  // relative to sequence start
+    const int row = w.q0 + r;        // query row, relative to the sequence's first query
+    const int pos = w.offset + row;  // its key position
     float m_used = -INFINITY, l = 0.f;
     if (p.sinks) {
       m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
@@ -482,12 +489,12 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       ++s_cnt;
       tc_fence_after();
       const int kbase = kt * kTileN;
-      const bool edge = (kbase + kTileN - 1 > w.q0) ||
-                        (p.window > 0 && kbase < w.q0 + kTileM - p.window);
+      const bool edge = (kbase + kTileN - 1 > w.offset + w.q0) ||
+                        (p.window > 0 && kbase < w.offset + w.q0 + kTileM - p.window);
       ChunkMask cm{0u, 0u};
-      if (edge) cm = classify_chunks(w.q0 + wq * 32, kbase, p.window);
-      const int hi_c = row - kbase;
-      const int lo_c = p.window > 0 ? row - p.window + 1 - kbase : -1;
+      if (edge) cm = classify_chunks(w.offset + w.q0 + wq * 32, kbase, p.window);
+      const int hi_c = pos - kbase;
+      const int lo_c = p.window > 0 ? pos - p.window + 1 - kbase : -1;
       // The row's 128 scores are processed as two halves of 64 columns, so
       // that at most one half of scores and the packed P of the other are
       // held in registers at a time.

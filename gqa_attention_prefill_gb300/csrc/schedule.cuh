@@ -1,10 +1,12 @@
-// Varlen scheduler pre-pass: one CTA turns cu_seqlens into the list of query
-// tiles (128 query rows of one sequence), each with its key-tile range, sorted
-// by cost (number of key tiles) in descending order, so that the persistent
-// attention kernel hands out the longest work first (longest-processing-time
-// order).  It also checks cu_seqlens: cu[0] == 0, non-decreasing,
-// cu[num_seqs] == total_tokens; on failure it records TSK_ERR_BAD_SEQLENS and
-// publishes an empty list.
+// Varlen scheduler pre-pass: one CTA turns the sequence offsets into the list
+// of query tiles (128 query rows of one sequence), each with its key-tile
+// range, sorted by cost (number of key tiles) in descending order, so that
+// the persistent attention kernel hands out the longest work first
+// (longest-processing-time order).  Sequence s has Lq = cu[s+1] - cu[s]
+// queries and Lk = cu_k[s+1] - cu_k[s] >= Lq keys; query i sits at key
+// position Lk - Lq + i (plain prefill: cu_k == cu).  It checks the offsets
+// (start at 0, non-decreasing, end at the totals, Lk >= Lq); on failure it
+// records TSK_ERR_BAD_SEQLENS and publishes an empty list.
 #pragma once
 #include <cstdint>
 
@@ -20,21 +22,27 @@ constexpr int kWsStatus = 0;   // [0] error code, [1] site, [2] block
 constexpr int kWsNTiles = 4;   // number of query tiles in the list
 constexpr int kWsHeader = 8;   // ints; tile offsets follow, then the int4 list (16-B aligned)
 
-struct QTile {   // one query tile
-  int start;     // first token of the sequence (absolute row)
-  int q0;        // first query row of the tile, relative to `start`
-  int kv_lo;     // first key tile (relative to `start`, in kTileN units)
-  int len;       // sequence length
-};
+// One query tile: two int4 per entry,
+//   {start_q, q0, kv_lo, len_q}  query start row, first query row of the tile
+//                                (relative to start_q), first key tile, Lq
+//   {start_k, offset, n_kv, 0}   key start row, Lk - Lq, number of key tiles
+constexpr int kTileEntryInts = 8;
 
-__device__ __forceinline__ int qtile_kv_lo(int q0, int window) {
-  if (window <= 0) return 0;
-  int lo = q0 - window + 1;
-  return lo > 0 ? lo / kTileN : 0;
+// Key tiles [kv_lo, kv_lo + n_kv) a query tile starting at q0 needs.
+__device__ __forceinline__ int2 qtile_key_range(int q0, int len_q, int offset, int window) {
+  const int last = (q0 + kTileM - 1 < len_q - 1 ? q0 + kTileM - 1 : len_q - 1);
+  const int kv_hi = (offset + last) / kTileN;
+  int kv_lo = 0;
+  if (window > 0) {
+    const int lo = offset + q0 - window + 1;
+    kv_lo = lo > 0 ? lo / kTileN : 0;
+  }
+  return make_int2(kv_lo, kv_hi - kv_lo + 1);
 }
 
 __global__ void __launch_bounds__(kSchedThreads, 1)
-    schedule_kernel(const int32_t* __restrict__ cu, int num_seqs, int total_tokens, int window,
+    schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k,
+                    int num_seqs, int total_tokens, int total_keys, int window,
                     int* __restrict__ ws, int* __restrict__ tile_off, int4* __restrict__ list,
                     int max_tiles) {
   __shared__ int s_scan[kSchedThreads];
@@ -43,7 +51,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   __shared__ int s_bad, s_base;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    s_bad = (cu[0] != 0 || cu[num_seqs] != total_tokens) ? 1 : 0;
+    s_bad = (cu[0] != 0 || cu[num_seqs] != total_tokens || cu_k[0] != 0 ||
+             cu_k[num_seqs] != total_keys) ? 1 : 0;
     s_base = 0;
   }
   for (int i = tid; i < kCostBins; i += kSchedThreads) {
@@ -58,7 +67,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     int nt = 0;
     if (s < num_seqs) {
       int L = cu[s + 1] - cu[s];
-      if (L < 0) {
+      const int Lk = cu_k[s + 1] - cu_k[s];
+      if (L < 0 || Lk < L) {
         s_bad = 1;
         L = 0;
       }
@@ -101,7 +111,9 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   for (int i = tid; i < n_tiles; i += kSchedThreads) {
     int s = seq_of(i);
     int qt = i - tile_off[s];
-    int cost = qt - qtile_kv_lo(qt * kTileM, window) + 1;
+    const int len = cu[s + 1] - cu[s];
+    const int cost =
+        qtile_key_range(qt * kTileM, len, (cu_k[s + 1] - cu_k[s]) - len, window).y;
     atomicAdd(&s_hist[min(cost, kCostBins) - 1], 1);
   }
   __syncthreads();
@@ -135,11 +147,13 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   for (int i = tid; i < n_tiles; i += kSchedThreads) {
     int s = seq_of(i);
     int qt = i - tile_off[s];
-    int q0 = qt * kTileM;
-    int kv_lo = qtile_kv_lo(q0, window);
-    int cost = qt - kv_lo + 1;
-    int pos = atomicAdd(&s_cursor[min(cost, kCostBins) - 1], 1);
-    list[pos] = make_int4(cu[s], q0, kv_lo, cu[s + 1] - cu[s]);
+    const int q0 = qt * kTileM;
+    const int len = cu[s + 1] - cu[s];
+    const int offset = (cu_k[s + 1] - cu_k[s]) - len;
+    const int2 kr = qtile_key_range(q0, len, offset, window);
+    const int pos = atomicAdd(&s_cursor[min(kr.y, kCostBins) - 1], 1);
+    list[2 * pos] = make_int4(cu[s], q0, kr.x, len);
+    list[2 * pos + 1] = make_int4(cu_k[s], offset, kr.y, 0);
   }
   if (tid == 0) ws[kWsNTiles] = n_tiles;
 }

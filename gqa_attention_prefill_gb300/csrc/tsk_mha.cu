@@ -133,7 +133,7 @@ tsk_status get_workspace(int dev, cudaStream_t stream, int max_tiles, int num_se
   mt = mt < 1024 ? 1024 : mt;
   ms = ms < 1024 ? 1024 : ms;
   size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ms + 1 + 3) & ~(size_t)3;
-  size_t bytes = off_ints * 4 + (size_t)mt * 16;
+  size_t bytes = off_ints * 4 + (size_t)mt * 4 * tsk::kTileEntryInts;
   int* nb = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -201,29 +201,38 @@ tsk_status tsk_debug_trace(unsigned long long* out, int32_t n) {
 
 int32_t tsk_kernels_per_call(void) { return 2; }
 
-tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const float* sinks,
-                           const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
-                           int32_t Hq, int32_t Hkv, int32_t D, int32_t window, float scale,
-                           void* out, float* lse, tsk_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+}  // extern "C"
+
+namespace {
+
+// Shared by tsk_mha_prefill (cu_k == cu_q, total_keys == total_queries) and
+// tsk_mha_prefill_kvcache.
+tsk_status prefill_impl(const void* q, const void* k, const void* v, const float* sinks,
+                        const int32_t* cu_q, const int32_t* cu_k, int32_t num_seqs,
+                        int64_t total_q, int64_t total_k, int32_t Hq, int32_t Hkv, int32_t D,
+                        int32_t window, float scale, void* out, float* lse,
+                        cudaStream_t stream, const char* what) {
   // ---- host-only checks (no CUDA call before these pass)
-  if (!q || !k || !v || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
-  if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !cu_q || !cu_k) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_q < 0 || total_k < 0 || Hq <= 0 || Hkv <= 0)
+    return TSK_ERR_INVALID_ARG;
+  if (total_k < total_q) return TSK_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
   if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
-  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
+  if (num_seqs >= (1 << 24) || total_q * (int64_t)Hq >= ((int64_t)1 << 31) ||
+      total_k * (int64_t)Hkv >= ((int64_t)1 << 31))
     return TSK_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
   if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return TSK_ERR_ALIGNMENT;
-  if (!a4(cu_seqlens) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
-  const size_t qo_bytes = (size_t)total_tokens * Hq * D * 2;
-  const size_t kv_bytes = (size_t)total_tokens * Hkv * D * 2;
-  if (total_tokens > 0 && (overlaps(out, qo_bytes, q, qo_bytes) ||
-                           overlaps(out, qo_bytes, k, kv_bytes) ||
-                           overlaps(out, qo_bytes, v, kv_bytes)))
+  if (!a4(cu_q) || !a4(cu_k) || (sinks && !a4(sinks)) || (lse && !a4(lse)))
+    return TSK_ERR_ALIGNMENT;
+  const size_t qo_bytes = (size_t)total_q * Hq * D * 2;
+  const size_t kv_bytes = (size_t)total_k * Hkv * D * 2;
+  if (total_q > 0 && (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k, kv_bytes) ||
+                      overlaps(out, qo_bytes, v, kv_bytes)))
     return TSK_ERR_INVALID_ARG;
-  if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
+  if (num_seqs == 0 || total_q == 0) return TSK_OK;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = -1;
@@ -232,20 +241,20 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
   if (st != TSK_OK) return st;
   if ((st = get_encoder()) != TSK_OK) return st;
 
-  const int64_t max_tiles64 = total_tokens / tsk::kTileM + num_seqs + 1;
+  const int64_t max_tiles64 = total_q / tsk::kTileM + num_seqs + 1;
   const int max_tiles = (int)max_tiles64;
   Workspace* ws = nullptr;
   if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
 
   CUtensorMap tq, tk, tv, to;
-  if ((st = encode_thd(&tq, q, total_tokens, Hq)) != TSK_OK) return st;
-  if ((st = encode_thd(&tk, k, total_tokens, Hkv)) != TSK_OK) return st;
-  if ((st = encode_thd(&tv, v, total_tokens, Hkv)) != TSK_OK) return st;
-  if ((st = encode_thd(&to, out, total_tokens, Hq, 32)) != TSK_OK) return st;
+  if ((st = encode_thd(&tq, q, total_q, Hq)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, total_k, Hkv)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, total_k, Hkv)) != TSK_OK) return st;
+  if ((st = encode_thd(&to, out, total_q, Hq, 32)) != TSK_OK) return st;
 
-  char name[96];
-  snprintf(name, sizeof name, "tsk_mha_prefill[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,T=%lld]", Hq, Hkv,
-           D, window, num_seqs, (long long)total_tokens);
+  char name[112];
+  snprintf(name, sizeof name, "%s[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,Tq=%lld,Tk=%lld]", what, Hq,
+           Hkv, D, window, num_seqs, (long long)total_q, (long long)total_k);
   nvtxRangePushA(name);
 
   const size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ws->max_seqs + 1 + 3) & ~(size_t)3;
@@ -269,7 +278,8 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
     cudaEventRecord(g_ev[0], stream);
   }
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
-      cu_seqlens, num_seqs, (int)total_tokens, window, ws->base, tile_off, list, ws->max_tiles);
+      cu_q, cu_k, num_seqs, (int)total_q, (int)total_k, window, ws->base, tile_off, list,
+      ws->max_tiles);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
   tsk::AttnParams p;
@@ -301,6 +311,30 @@ tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const fl
   }
   nvtxRangePop();
   return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+tsk_status tsk_mha_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                           const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                           int32_t Hq, int32_t Hkv, int32_t D, int32_t window, float scale,
+                           void* out, float* lse, tsk_stream_t stream) {
+  return prefill_impl(q, k, v, sinks, cu_seqlens, cu_seqlens, num_seqs, total_tokens,
+                      total_tokens, Hq, Hkv, D, window, scale, out, lse,
+                      reinterpret_cast<cudaStream_t>(stream), "tsk_mha_prefill");
+}
+
+tsk_status tsk_mha_prefill_kvcache(const void* q, const void* k, const void* v,
+                                   const float* sinks, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                   int64_t total_q, int64_t total_k, int32_t Hq, int32_t Hkv,
+                                   int32_t D, int32_t window, float scale, void* out,
+                                   float* lse, tsk_stream_t stream) {
+  return prefill_impl(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                      Hq, Hkv, D, window, scale, out, lse,
+                      reinterpret_cast<cudaStream_t>(stream), "tsk_mha_prefill_kvcache");
 }
 
 tsk_status tsk_get_device_status(tsk_stream_t stream_) {
@@ -382,7 +416,8 @@ constexpr int kNoAllocMaxSeqs = 16384;    // sequences per call
 constexpr int kNoAllocMaxTiles = 49152;   // total_tokens/128 + num_seqs + 1, at most
 constexpr size_t kNoAllocOffInts =
     ((size_t)tsk::kWsHeader + (size_t)kNoAllocMaxSeqs + 1 + 3) & ~(size_t)3;
-constexpr size_t kNoAllocBytes = kNoAllocOffInts * 4 + (size_t)kNoAllocMaxTiles * 16;  // ~0.85 MB
+constexpr size_t kNoAllocBytes =
+    kNoAllocOffInts * 4 + (size_t)kNoAllocMaxTiles * 4 * tsk::kTileEntryInts;  // ~1.6 MB
 
 static __device__ __align__(256) int g_noalloc_scratch[kNoAllocBytes / 4];
 
@@ -453,8 +488,8 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   cudaError_t e = cudaMemsetAsync(scratch, 0, tsk::kWsHeader * sizeof(int), stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch header");
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
-      cu_seqlens, num_seqs, (int)total_tokens, window, scratch, tile_off, list,
-      kNoAllocMaxTiles);
+      cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, scratch,
+      tile_off, list, kNoAllocMaxTiles);
 
   tsk::AttnParams p;
   p.sinks = sinks;

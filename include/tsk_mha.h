@@ -86,6 +86,35 @@ TSK_API tsk_status tsk_mha_prefill(const void *q, const void *k, const void *v, 
                            int32_t Hq, int32_t Hkv, int32_t D, int32_t window, float scale,
                            void *out, float *lse, tsk_stream_t stream);
 
+/*
+ * tsk_mha_prefill_kvcache -- prefill over a key/value cache (README, section
+ * "Public API": `mha_prefill_with_kvcache`; the pages give no formula).
+ * Sequence s has Lq = cu_seqlens_q[s+1] - cu_seqlens_q[s] new query tokens
+ * and Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s] >= Lq keys/values: the cached
+ * prefix followed by the new tokens' own keys/values.  New token i sits at
+ * key position P = Lk - Lq + i and attends to key positions
+ * max(0, P - W + 1) .. P of its own sequence (causal aligned to the end of
+ * the keys); otherwise as tsk_mha_prefill (sinks, scale, lse, GQA mapping).
+ * With Lk == Lq for every sequence this is tsk_mha_prefill.
+ *
+ *   q             device, bf16 [total_q, Hq, D]
+ *   k, v          device, bf16 [total_k, Hkv, D] (contiguous per sequence)
+ *   cu_seqlens_q  device, int32 [num_seqs + 1], 0 .. total_q, non-decreasing
+ *   cu_seqlens_k  device, int32 [num_seqs + 1], 0 .. total_k, non-decreasing
+ *   total_q, total_k  host copies of the last offsets (total_k >= total_q)
+ *   out           device, bf16 [total_q, Hq, D]; lse fp32 [total_q, Hq] or NULL
+ *
+ * Inconsistent offsets (including Lk < Lq for some sequence) are reported as
+ * TSK_ERR_BAD_SEQLENS through tsk_get_device_status and nothing is computed.
+ * Limits: total_q * Hq < 2^31 and total_k * Hkv < 2^31.
+ */
+TSK_API tsk_status tsk_mha_prefill_kvcache(const void *q, const void *k, const void *v,
+                                           const float *sinks, const int32_t *cu_seqlens_q,
+                                           const int32_t *cu_seqlens_k, int32_t num_seqs,
+                                           int64_t total_q, int64_t total_k, int32_t Hq,
+                                           int32_t Hkv, int32_t D, int32_t window, float scale,
+                                           void *out, float *lse, tsk_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 TSK_API const char *tsk_status_string(tsk_status s);
 
@@ -151,7 +180,7 @@ TSK_API tsk_status tsk_debug_trace(unsigned long long *out, int32_t n);
  *
  * It calls no cudaMalloc/cudaFree or other allocating routine.  Its scratch
  * (status words, tile offsets, the sorted query-tile list) is a fixed
- * ~0.85 MB array in the library's device memory, which every GPU that loads
+ * ~1.6 MB array in the library's device memory, which every GPU that loads
  * the library holds until the process exits.  Limits: num_seqs <= 16384 and
  * total_tokens/128 + num_seqs + 1 <= 49152; larger problems are rejected with
  * TSK_ERR_UNSUPPORTED (tsk_last_error says which limit) before anything is

@@ -23,6 +23,8 @@ def to_device(w: inputgen.Workload, device="cuda"):
         "cu": torch.from_numpy(w.cu_seqlens).to(device),
         "sinks": None if w.sinks is None else torch.from_numpy(w.sinks).to(device),
     }
+    if w.cu_seqlens_k is not None:
+        d["cu_k"] = torch.from_numpy(w.cu_seqlens_k).to(device)
     return d
 
 
@@ -35,8 +37,13 @@ def run_gpu(w: inputgen.Workload, d=None, with_lse=True, check_status=True):
     out = torch.full((T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=d["q"].device)
     lse = torch.full((T, w.Hq), float("nan"), dtype=torch.float32, device=d["q"].device) \
         if with_lse else None
-    rc = pkg.tsk_mha_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu"], w.num_seqs, T, w.Hq,
-                             w.Hkv, w.D, w.window, w.scale, out, lse)
+    if w.cu_seqlens_k is not None:
+        rc = pkg.tsk_mha_prefill_kvcache(d["q"], d["k"], d["v"], d["sinks"], d["cu"], d["cu_k"],
+                                         w.num_seqs, T, w.total_keys, w.Hq, w.Hkv, w.D, w.window,
+                                         w.scale, out, lse)
+    else:
+        rc = pkg.tsk_mha_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu"], w.num_seqs, T,
+                                 w.Hq, w.Hkv, w.D, w.window, w.scale, out, lse)
     assert rc == 0, f"{pkg.STATUS.get(rc, rc)} {pkg.tsk_last_error()}"
     torch.cuda.synchronize()
     if check_status:

@@ -91,3 +91,27 @@ def test_host_side_rejections(lib, kw, code):
 @pytest.mark.parametrize("kw", [dict(num_seqs=0), dict(total_tokens=0)])
 def test_empty_problems_return_ok_without_launch(lib, kw):
     assert call(lib, **kw) == 0
+
+
+def kv_call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 3, v=FAKE * 5, sinks=None, cu=FAKE * 7, cu_k=FAKE * 13, num_seqs=1,
+             total_q=128, total_k=512, Hq=8, Hkv=2, D=64, window=0, scale=0.125, out=FAKE * 9,
+             lse=None)
+    a.update(kw)
+    return lib.tsk_mha_prefill_kvcache(a["q"], a["k"], a["v"], a["sinks"], a["cu"], a["cu_k"],
+                                       a["num_seqs"], a["total_q"], a["total_k"], a["Hq"],
+                                       a["Hkv"], a["D"], a["window"], a["scale"], a["out"],
+                                       a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_k=None), -1), (dict(total_k=100), -1), (dict(total_k=-1), -1), (dict(D=128), -2),
+    (dict(cu_k=FAKE * 13 + 2), -3), (dict(total_k=(1 << 30), Hkv=2), -2),
+    (dict(out=FAKE * 3 + 16), -1),
+])
+def test_kvcache_host_side_rejections(lib, kw, code):
+    assert kv_call(lib, **kw) == code
+
+
+def test_kvcache_empty_returns_ok(lib):
+    assert kv_call(lib, total_q=0, total_k=0) == 0
