@@ -53,9 +53,9 @@ constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // 16 KB (also K/V tiles
 constexpr uint32_t kSmemQ = 0;                           // 2 buffers x 2 tiles
 constexpr uint32_t kSmemKV = 4 * kTileBytes;             // kStages x (K, V)
 constexpr uint32_t kSmemBar = kSmemKV + kStages * 2 * kTileBytes;  // barriers (< 512 B)
-constexpr uint32_t kSmemEpi = kSmemBar + 1024;  // 2 output staging tiles (small-window kernel)
+constexpr uint32_t kSmemEpi = kSmemBar + 1024;  // 2 output staging tiles
 // Dynamic shared memory per kernel variant, + 1 KB slack for the alignment.
-constexpr uint32_t kSmemBytesCausal = kSmemBar + 512 + 1024;
+constexpr uint32_t kSmemBytesCausal = kSmemEpi + 2 * kTileBytes + 1024;
 constexpr uint32_t kSmemBytesWindow = kSmemEpi + 2 * kTileBytes + 1024;
 
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
@@ -130,6 +130,17 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   r.ntiles = (2 * hp + 1 < p.G) ? 2 : 1;
   return r;
 }
+
+// The unit's sequence fields read again (volatile loads: not merged with the
+// first read), so that they need no registers while a unit's key tiles run.
+__device__ __forceinline__ int4 ld_nc_v4_volatile(const int4* a) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(a));
+  return v;
+}
+
 
 // State shared by the roles of one CTA.
 struct Ctx {
@@ -294,7 +305,7 @@ __device__ __forceinline__ ChunkMask classify_chunks(int row0, int kbase, int wi
 // exponentials), edge tiles are masked per element, and each thread stores
 // its output row directly.
 __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnParams& p,
-                                                    int warp, int lane) {
+                                                    const CUtensorMap* tmO, int warp, int lane) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;          // TMEM lane quarter
   const int r = wq * 32 + lane;     // query row within the tile
@@ -302,24 +313,33 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   const uint32_t tS = cx.tmem + lane_base + kColS0 + 128 * t;
   const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
   const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
+  const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
   uint32_t s_cnt = 0, pv_cnt = 0;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
-    if (t >= w.ntiles) continue;
-    const int h = w.h0 + t;
-    const int row = w.q0 + r;        // query row, relative to the sequence's first query
-    const int pos = w.offset + row;  // its key position
+    TSK_TRACE_T0(tr_dec);
+    // Only what the key loop needs is kept from the unit; the epilogue reads
+    // the sequence fields again (registers are the scarce resource here).
+    int n_kv, kv_lo, diag0, pos;
     float m_used = -INFINITY, l = 0.f;
-    if (p.sinks) {
-      m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
-      l = 1.f;
+    {
+      const Unit w = decode_unit(p, u);
+      if (t >= w.ntiles) continue;
+      n_kv = w.n_kv;
+      kv_lo = w.kv_lo;
+      diag0 = w.offset + w.q0;  // key position of the tile's first query row
+      pos = diag0 + r;          // key position of this thread's query row
+      if (p.sinks) {
+        m_used = __ldg(p.sinks + w.h0 + t) * 1.4426950408889634f;
+        l = 1.f;
+      }
     }
-    for (int j = 0; j < w.n_kv; ++j) {
-      const int kt = w.kv_lo + j;
-      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, 9, p, cx.abort);
+    TSK_TRACE_ADD(24, tr_dec);
+    for (int j = 0; j < n_kv; ++j) {
+      const int kt = kv_lo + j;
+      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort);
       if (!ok) break;
       ++s_cnt;
       tc_fence_after();
@@ -339,15 +359,28 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       const int kbase = kt * kTileN;
-      const bool edge = (kbase + kTileN - 1 > w.offset + w.q0) ||
-                        (p.window > 0 && kbase < w.offset + w.q0 + kTileM - p.window);
+      const bool edge = (kbase + kTileN - 1 > diag0) ||
+                        (p.window > 0 && kbase < diag0 + kTileM - p.window);
+      TSK_TRACE_T0(tr_mask);
       if (edge) {
+        // Only 32-key chunks partly visible to this warp need a per-element
+        // test; chunks hidden from all of its rows are cleared whole.
+        const ChunkMask cm = classify_chunks(diag0 + wq * 32, kbase, p.window);
         const int hi_c = pos - kbase;
         const int lo_c = p.window > 0 ? pos - p.window + 1 - kbase : -1;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > hi_c || c < lo_c) s[c] = -INFINITY;
+        for (int k = 0; k < 4; ++k) {
+          if (cm.partial & (1u << k)) {
+#pragma unroll
+            for (int c = 32 * k; c < 32 * k + 32; ++c)
+              s[c] = (c > hi_c || c < lo_c) ? -INFINITY : s[c];
+          } else if (cm.none & (1u << k)) {
+#pragma unroll
+            for (int c = 32 * k; c < 32 * k + 32; ++c) s[c] = -INFINITY;
+          }
+        }
       }
+      TSK_TRACE_ADD(27, tr_mask);
       // Row maximum: four independent chains of 3-input max.
       TSK_TRACE_T0(tr_max);
       float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
@@ -373,10 +406,10 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       TSK_TRACE_T0(tr_exp);
       // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per element,
       // four scalar partial sums, bf16x2 packing for TMEM.
+      uint32_t pk[64];
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm = f2_pack(-m_use, -m_use);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         float x0, x1;
@@ -417,7 +450,13 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     }
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
-    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
+    const int per_tile = p.Hkv * p.HP;
+    const int qi = u / per_tile;
+    const int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
+    const int g = (u - qi * per_tile) / p.HP;
+    const int h = g * p.G + 2 * (u - qi * per_tile - g * p.HP) + t;
+    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
+    TSK_TRACE_T0(tr_epi);
     if (!ok) break;
     ++pv_cnt;
     tc_fence_after();
@@ -426,24 +465,40 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     tmem_ld_32x32b_x32(tO + 32, o + 32);
     tmem_wait_ld();
     reg_fence<64>(o);
-    if (row < w.len) {
-      const float inv = 1.f / l;
-      const size_t orow = (size_t)(w.start + row) * p.Hq + h;
+    const float inv = rcp_approx(l);
+    uint32_t ob[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+    const int row = e.y + r;  // query row, relative to the sequence's first query
+    const size_t orow = (size_t)(e.x + row) * p.Hq + h;
+    if (p.lse && row < e.w) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    if (e.y + wq * 32 + 32 <= e.w) {
+      // The warp's 32 rows lie inside the sequence: stage them in this warp's
+      // slice of the staging tile and store them with one TMA bulk store.
+      if (lane == 0) bulk_wait_group_read0();  // the warp's previous store has read its slice
+      __syncwarp();
+      const uint32_t dst_row = epi + (uint32_t)r * 128u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(dst_row + ((uint32_t)(c ^ (r & 7)) << 4), ob[4 * c], ob[4 * c + 1],
+                     ob[4 * c + 2], ob[4 * c + 3]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, e.x + e.y + wq * 32);
+        bulk_commit_group();
+      }
+    } else if (row < e.w) {
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-        v.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-        v.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-        v.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-        dst[c] = v;
-      }
-      if (p.lse) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+      for (int c = 0; c < 8; ++c)
+        dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
     }
     tc_fence_before();
+    TSK_TRACE_ADD(28, tr_epi);
   }
-
+  if (lane == 0) bulk_wait_group0();  // every output store of this warp has completed
   TSK_TRACE_ADD(30, tr_all);
 }
 
@@ -733,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   else if (warp == 2 && lane == 0) role_mma(cx, p, 1);
   else if (warp >= kFirstSoftmaxWarp) {
     if constexpr (kSmallWindow) role_softmax_window(cx, p, &tmO, warp, lane);
-    else role_softmax_causal(cx, p, warp, lane);
+    else role_softmax_causal(cx, p, &tmO, warp, lane);
   }
 
   // ------------------------------------------------------------------ teardown
