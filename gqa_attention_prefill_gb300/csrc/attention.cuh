@@ -223,6 +223,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
     if (!ok) break;
     const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes;
     auto issue_s = [&](int stage) {
+      TSK_TRACE_T0(tr_is);
       const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
@@ -230,6 +231,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
                kk > 0 ? 1u : 0u);
       tc_commit(cx.bar(kBarSFull + t));
       ++s_cnt;
+      TSK_TRACE_ADD(15, tr_is);
     };
     {  // S_t(0)
       const int s0 = kv_iter % kStages;
@@ -255,12 +257,14 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       if (!ok) break;
       tc_fence_after();
       const uint32_t b = cx.sbase + kSmemKV + sc * 2 * kTileBytes + kTileBytes;
+      TSK_TRACE_T0(tr_ip);
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk)
         mma_ts(d_o, a_p + 8 * kk, sdesc_sw128(b + 2048 * kk), kIdescPV,
                (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(cx.bar(kBarPVDone + t));
       ++p_cnt;
+      TSK_TRACE_ADD(16, tr_ip);
       for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarKVEmpty + sc));
     }
     if (!ok) break;
