@@ -166,8 +166,8 @@ def tsk_mha_prefill_kvcache(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k, num_seqs
 def mha_prefill_kvcache(q, k, v, cu_seqlens_q, cu_seqlens_k, sinks=None, window: int = 0,
                         scale: float | None = None, out=None, lse=None, return_lse=True,
                         stream=None):
-    """Tensor-level convenience over ``tsk_mha_prefill_kvcache``: q [Tq, Hq, 64],
-    k/v [Tk, Hkv, 64] bf16 CUDA, int32 CUDA offsets.  Returns (out, lse)."""
+    """Tensor-level convenience over ``tsk_mha_prefill_kvcache``: q [Tq, Hq, D],
+    k/v [Tk, Hkv, D] bf16 CUDA (D = 64 or 128), int32 CUDA offsets.  Returns (out, lse)."""
     import torch
     Tq, Hq, D = q.shape
     Tk, Hkv = k.shape[0], k.shape[1]
@@ -199,9 +199,9 @@ def mha_prefill(q, k, v, cu_seqlens, sinks=None, window: int = 0, scale: float |
                 out=None, lse=None, return_lse: bool = True, stream=None):
     """Tensor-level convenience over ``tsk_mha_prefill``.
 
-    q: [T, Hq, 64] bf16 CUDA; k, v: [T, Hkv, 64] bf16 CUDA; cu_seqlens: int32
+    q: [T, Hq, D] bf16 CUDA; k, v: [T, Hkv, D] bf16 CUDA (D = 64 or 128); cu_seqlens: int32
     CUDA [num_seqs+1]; sinks: fp32 CUDA [Hq] or None.  Returns (out, lse) with
-    out [T, Hq, 64] bf16 and lse [T, Hq] fp32 (None if return_lse is False).
+    out [T, Hq, D] bf16 and lse [T, Hq] fp32 (None if return_lse is False).
     """
     import torch
     T, Hq, D = q.shape

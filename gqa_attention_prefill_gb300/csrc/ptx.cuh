@@ -17,6 +17,27 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- timeline
+// Builds with -DTSK_TIMELINE record, for block 0 only, a per-warp list of
+// (event id, clock64) pairs into g_tsk_tl (lane 0 of each warp; plain stores,
+// no read-modify-write), read back by tsk_debug_timeline().  A role function
+// declares its event counter with TSK_TL_DECL and records with TSK_EV(id).
+constexpr int kTlWarps = 16;
+constexpr int kTlCap = 16384;
+#ifdef TSK_TIMELINE
+__device__ unsigned long long g_tsk_tl[kTlWarps][kTlCap];
+#define TSK_TL_DECL int tsk_tl_i = 0
+#define TSK_EV(id)                                                                           \
+  do {                                                                                       \
+    if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && tsk_tl_i < kTlCap)                     \
+      g_tsk_tl[threadIdx.x >> 5][tsk_tl_i++] =                                               \
+          ((unsigned long long)(id) << 56) | ((unsigned long long)clock64() & 0xFFFFFFFFFFFFFFull); \
+  } while (0)
+#else
+#define TSK_TL_DECL
+#define TSK_EV(id)
+#endif
+
 // ----------------------------------------------------------------- tracing
 // Builds with -DTSK_TRACE accumulate clock64() cycles per code site (lane 0 of
 // each warp, in shared memory, flushed once at kernel exit) into

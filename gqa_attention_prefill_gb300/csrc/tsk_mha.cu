@@ -15,6 +15,7 @@
 
 #include "tsk_mha.h"
 #include "attention.cuh"
+#include "attention_d128.cuh"
 #include "schedule.cuh"
 
 namespace {
@@ -72,11 +73,13 @@ tsk_status get_encoder() {
   return TSK_OK;
 }
 
-// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token); box = 64 x 1 x
-// box_rows rows of 128 bytes, stored with the 128-byte swizzle.
-tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int box_rows = 128) {
-  cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {64 * 2, (cuuint64_t)H * 64 * 2};
+// [T, H, D] bf16 viewed as a 3-D tensor (d, head, token); box = 64 x 1 x
+// box_rows: rows of 128 bytes (64 of the D columns), stored with the 128-byte
+// swizzle.  D = 128 rows are read as two boxes at d = 0 and d = 64.
+tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int D,
+                      int box_rows = 128) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
@@ -113,6 +116,10 @@ tsk_status check_device(int* dev_out, DeviceState** st_out) {
       e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::kSmemBytesWindow);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::d128::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     st.smem_set = true;
   }
@@ -199,11 +206,45 @@ tsk_status tsk_debug_trace(unsigned long long* out, int32_t n) {
 #endif
 }
 
+tsk_status tsk_debug_timeline(unsigned long long* out, int32_t n) {
+#ifdef TSK_TIMELINE
+  if (!out || n <= 0) return TSK_ERR_INVALID_ARG;
+  const size_t total = (size_t)tsk::kTlWarps * tsk::kTlCap;
+  const size_t m = (size_t)n < total ? (size_t)n : total;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(out, tsk::g_tsk_tl, m * 8);
+  if (e != cudaSuccess) return cuda_fail(e, "timeline read");
+  static unsigned long long zero[tsk::kTlCap] = {};
+  for (int w = 0; w < tsk::kTlWarps && e == cudaSuccess; ++w)
+    e = cudaMemcpyToSymbol(tsk::g_tsk_tl, zero, sizeof zero, (size_t)w * sizeof zero);
+  return e == cudaSuccess ? TSK_OK : cuda_fail(e, "timeline clear");
+#else
+  (void)out;
+  (void)n;
+  return TSK_ERR_UNSUPPORTED;
+#endif
+}
+
 int32_t tsk_kernels_per_call(void) { return 2; }
 
 }  // extern "C"
 
 namespace {
+
+// The attention kernel for head dimension D (64 or 128) and the window.
+void launch_attention(int D, int window, int grid, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const CUtensorMap& to, const tsk::AttnParams& p,
+                      cudaStream_t stream) {
+  if (D == 128)
+    tsk::d128::attention_fwd_d128_kernel<<<grid, tsk::kThreads, tsk::d128::kSmemBytes, stream>>>(
+        tq, tk, tv, to, p);
+  else if (window > 0 && window <= tsk::kSmallWindowMax)
+    tsk::attention_fwd_kernel<true><<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(
+        tq, tk, tv, to, p);
+  else
+    tsk::attention_fwd_kernel<false><<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(
+        tq, tk, tv, to, p);
+}
 
 // Shared by tsk_mha_prefill (cu_k == cu_q, total_keys == total_queries) and
 // tsk_mha_prefill_kvcache.
@@ -218,7 +259,7 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
     return TSK_ERR_INVALID_ARG;
   if (total_k < total_q) return TSK_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
-  if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if ((D != 64 && D != 128) || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
   if (num_seqs >= (1 << 24) || total_q * (int64_t)Hq >= ((int64_t)1 << 31) ||
       total_k * (int64_t)Hkv >= ((int64_t)1 << 31))
     return TSK_ERR_UNSUPPORTED;
@@ -247,10 +288,10 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
 
   CUtensorMap tq, tk, tv, to;
-  if ((st = encode_thd(&tq, q, total_q, Hq)) != TSK_OK) return st;
-  if ((st = encode_thd(&tk, k, total_k, Hkv)) != TSK_OK) return st;
-  if ((st = encode_thd(&tv, v, total_k, Hkv)) != TSK_OK) return st;
-  if ((st = encode_thd(&to, out, total_q, Hq, 32)) != TSK_OK) return st;
+  if ((st = encode_thd(&tq, q, total_q, Hq, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, total_k, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, total_k, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&to, out, total_q, Hq, D, 32)) != TSK_OK) return st;
 
   char name[112];
   snprintf(name, sizeof name, "%s[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,Tq=%lld,Tk=%lld]", what, Hq,
@@ -299,10 +340,7 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   p.debug_stall = g_debug_stall;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  if (window > 0 && window <= tsk::kSmallWindowMax)
-    tsk::attention_fwd_kernel<true><<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(tq, tk, tv, to, p);
-  else
-    tsk::attention_fwd_kernel<false><<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(tq, tk, tv, to, p);
+  launch_attention(D, window, grid, tq, tk, tv, to, p, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) note_error("attention kernel launch", e);
   if (prof) {
@@ -436,7 +474,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   if (!q || !k || !v || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
   if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
-  if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if ((D != 64 && D != 128) || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
   if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
     return TSK_ERR_UNSUPPORTED;
   const int64_t max_tiles64 = total_tokens / tsk::kTileM + num_seqs + 1;
@@ -476,10 +514,10 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   }
 
   CUtensorMap tq, tk, tv, to;
-  if ((st = encode_thd(&tq, q, total_tokens, Hq)) != TSK_OK) return st;
-  if ((st = encode_thd(&tk, k, total_tokens, Hkv)) != TSK_OK) return st;
-  if ((st = encode_thd(&tv, v, total_tokens, Hkv)) != TSK_OK) return st;
-  if ((st = encode_thd(&to, out, total_tokens, Hq, 32)) != TSK_OK) return st;
+  if ((st = encode_thd(&tq, q, total_tokens, Hq, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, total_tokens, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, total_tokens, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&to, out, total_tokens, Hq, D, 32)) != TSK_OK) return st;
 
   int* tile_off = scratch + tsk::kWsHeader;
   int4* list = reinterpret_cast<int4*>(scratch + kNoAllocOffInts);
@@ -508,10 +546,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   p.debug_stall = 0;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  if (window > 0 && window <= tsk::kSmallWindowMax)
-    tsk::attention_fwd_kernel<true><<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(tq, tk, tv, to, p);
-  else
-    tsk::attention_fwd_kernel<false><<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(tq, tk, tv, to, p);
+  launch_attention(D, window, grid, tq, tk, tv, to, p, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     note_error("attention kernel launch (no-alloc)", e);

@@ -41,7 +41,7 @@ typedef struct CUstream_st *tsk_stream_t; /* a cudaStream_t; NULL = legacy defau
 typedef enum {
   TSK_OK = 0,
   TSK_ERR_INVALID_ARG = -1,    /* NULL where a buffer is required, negative sizes, bad scale */
-  TSK_ERR_UNSUPPORTED = -2,    /* D != 64, Hq % Hkv != 0, sizes beyond the limits below */
+  TSK_ERR_UNSUPPORTED = -2,    /* D not 64 or 128, Hq % Hkv != 0, sizes beyond the limits below */
   TSK_ERR_ALIGNMENT = -3,      /* q/k/v/out not 16-byte aligned, sinks/lse/cu not 4-byte */
   TSK_ERR_DEVICE = -4,         /* no device, not compute capability 10.3, CUDA error */
   TSK_ERR_OOM = -5,            /* workspace allocation failed */
@@ -65,7 +65,7 @@ typedef enum {
  *               TSK_ERR_BAD_SEQLENS through tsk_get_device_status on mismatch,
  *               computing nothing in that case)
  *   Hq, Hkv     query / KV heads; Hq % Hkv == 0 (Hq == Hkv is plain MHA)
- *   D           head dimension; must be 64
+ *   D           head dimension: 64 (GPT-OSS shapes) or 128 (its own kernel)
  *   window      <= 0: full causal; W >= 1: token t sees keys t-W+1 .. t
  *   scale       multiplier of q.k (finite, > 0); not applied to sinks
  *   out         device, bf16 [total_tokens, Hq, D]; must not overlap q, k, v
@@ -168,6 +168,15 @@ TSK_API tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall);
  * launch.
  */
 TSK_API tsk_status tsk_debug_trace(unsigned long long *out, int32_t n);
+
+/*
+ * tsk_debug_timeline -- libraries built with -DTSK_TIMELINE only (otherwise
+ * TSK_ERR_UNSUPPORTED): copies up to n entries of block 0's event record of
+ * the last launch into host memory `out` and clears it.  Entry
+ * [warp * 16384 + i] is event i of that warp: id in bits 56..63, SM clock in
+ * bits 0..55; unused entries are 0.  Synchronises the device.
+ */
+TSK_API tsk_status tsk_debug_timeline(unsigned long long *out, int32_t n);
 
 /*
  * tsk_mha_prefill_noalloc -- the same operation and arguments as

@@ -203,6 +203,11 @@ CONFIGS = {
     # prefill over a key/value cache (not one of the five above)
     "kvcache_4x2048_on_4096_h64kv8": dict(desc="4 seqs x 2048 new tokens over a 4096-token cache "
                                                "(Lk = 6144), Hq=64, Hkv=8, D=64, causal"),
+    # head dimension 128 (the same unmasked FLOPs as causal_4x4096_h64kv8)
+    "causal_4x4096_h32kv8_d128": dict(desc="4 seqs x 4096 tokens, Hq=32, Hkv=8, D=128, "
+                                           "sinks N(0,1), scale 1/sqrt(128), full causal"),
+    "long_1x32768_h32kv8_d128": dict(desc="1 seq x 32768 tokens, Hq=32, Hkv=8, D=128, "
+                                          "K = bf16(3*N(0,1)), scale 1/sqrt(128), full causal"),
 }
 
 
@@ -225,6 +230,10 @@ def config(name: str, seed: int = 0) -> Workload:
         return make([32768], 64, 8, k_mult=3.0, seed=seed, name=name)
     if name == "kvcache_4x2048_on_4096_h64kv8":
         return make_kvcache([2048] * 4, [6144] * 4, 64, 8, seed=seed, name=name)
+    if name == "causal_4x4096_h32kv8_d128":
+        return make([4096] * 4, 32, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
+    if name == "long_1x32768_h32kv8_d128":
+        return make([32768], 32, 8, D=128, scale=128 ** -0.5, k_mult=3.0, seed=seed, name=name)
     raise KeyError(name)
 
 

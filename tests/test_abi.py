@@ -76,7 +76,7 @@ def call(lib, **kw):
     (dict(cu=None), -1), (dict(num_seqs=-1), -1), (dict(total_tokens=-5), -1),
     (dict(Hq=0), -1), (dict(Hkv=0), -1), (dict(scale=0.0), -1), (dict(scale=-1.0), -1),
     (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
-    (dict(D=128), -2), (dict(D=32), -2), (dict(Hq=6, Hkv=4), -2),
+    (dict(D=96), -2), (dict(D=32), -2), (dict(Hq=6, Hkv=4), -2),
     (dict(total_tokens=1 << 26, Hq=64), -2), (dict(num_seqs=1 << 24), -2),
     (dict(q=FAKE + 8), -3), (dict(k=FAKE * 3 + 2), -3), (dict(v=FAKE * 5 + 4), -3),
     (dict(out=FAKE * 9 + 1), -3), (dict(cu=FAKE * 7 + 2), -3), (dict(sinks=FAKE + 1), -3),
@@ -105,7 +105,7 @@ def kv_call(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(cu_k=None), -1), (dict(total_k=100), -1), (dict(total_k=-1), -1), (dict(D=128), -2),
+    (dict(cu_k=None), -1), (dict(total_k=100), -1), (dict(total_k=-1), -1), (dict(D=256), -2),
     (dict(cu_k=FAKE * 13 + 2), -3), (dict(total_k=(1 << 30), Hkv=2), -2),
     (dict(out=FAKE * 3 + 16), -1),
 ])
