@@ -396,7 +396,9 @@ def main():
                      "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name),
                      "peak_source": f"{peak_src} dense bf16 (burst)",
                      "algorithmic_bytes": w.algorithmic_bytes(),
-                     "kernel": "attention_fwd_kernel"},
+                     "kernel": ("attention_fwd_d128_kernel" if D == 128 else
+                                "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
+                                "attention_fwd_kernel<false>")},
         "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "matches_resident_run": bool(same)},

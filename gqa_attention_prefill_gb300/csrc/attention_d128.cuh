@@ -465,10 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   cx.abort = smem_u32(const_cast<int*>(abort_flag));
   cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
 
-  if (warp == 0 && lane == 0) d128::role_producer(cx, &tmQ, &tmK, &tmV, p);
-  else if (warp == 1 && lane == 0) d128::role_mma(cx, p, 0);
-  else if (warp == 2 && lane == 0) d128::role_mma(cx, p, 1);
-  else if (warp >= kFirstSoftmaxWarp) d128::role_softmax(cx, p, &tmO, warp, lane);
+  // Registers move from the producer/MMA warpgroup (56 each) to the softmax
+  // warpgroups (224 each): 128 x 56 + 256 x 224 = 384 x 168, the launch's total.
+  if (warp < kFirstSoftmaxWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0 && lane == 0) d128::role_producer(cx, &tmQ, &tmK, &tmV, p);
+    else if (warp == 1 && lane == 0) d128::role_mma(cx, p, 0);
+    else if (warp == 2 && lane == 0) d128::role_mma(cx, p, 1);
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    d128::role_softmax(cx, p, &tmO, warp, lane);
+  }
 
   __syncwarp();
   tc_fence_before();
