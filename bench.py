@@ -63,15 +63,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(D=64):
+    """Hash of the device sources the attention kernel for head dimension D is
+    built from (the host file and the other head dimension's kernel excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_attention_prefill_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = ["ptx.cuh", "schedule.cuh", "attention.cuh"] + (["attention_d128.cuh"] if D == 128 else [])
+    for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
+def ncu_traffic(workload, D=64):
     """Per-launch DRAM bytes of the attention kernel from a committed ncu
     summary, if it was taken on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -80,7 +83,7 @@ def ncu_traffic(workload):
     try:
         d = json.load(open(p))
         e = d.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        if e and e.get("kernel_source_hash") == kernel_source_hash(D):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -393,7 +396,7 @@ def main():
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
         "roofline": {"bound": "tensor", "achieved": achieved,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name),
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name, D),
                      "peak_source": f"{peak_src} dense bf16 (burst)",
                      "algorithmic_bytes": w.algorithmic_bytes(),
                      "kernel": ("attention_fwd_d128_kernel" if D == 128 else
@@ -404,7 +407,7 @@ def main():
                 "matches_resident_run": bool(same)},
         "gpu_launches": args.steps * pkg.tsk_kernels_per_call(),
         "clocks": clk.summary(),
-        "kernel_source_hash": kernel_source_hash(),
+        "kernel_source_hash": kernel_source_hash(D),
     }
     if not args.no_cpu_baseline:
         r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds)
