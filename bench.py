@@ -279,6 +279,7 @@ def main():
     h_s = torch.from_numpy(w.sinks).pin_memory()
     h_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
     kvcache = w.cu_seqlens_k is not None
+    decode = kvcache and all(L == 1 for L in w.seqlens)  # one query token per sequence
     h_cuk = torch.from_numpy(w.cu_seqlens_k if kvcache else w.cu_seqlens).pin_memory()
     q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
     sinks, cu, cuk = h_s.to(dev), h_cu.to(dev), h_cuk.to(dev)
@@ -287,7 +288,11 @@ def main():
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def step(o=out, l=lse, qq=q, kk=k, vv=v, ss=sinks, cc=cu, ck=cuk):
-        if kvcache:
+        if decode:
+            rc = pkg.tsk_mha_decode_kvcache(qq, kk, vv, ss, ck, w.num_seqs, w.total_keys,
+                                            max(w.seqlens_k), Hq, Hkv, D, w.window, w.scale, o, l,
+                                            stream)
+        elif kvcache:
             rc = pkg.tsk_mha_prefill_kvcache(qq, kk, vv, ss, cc, ck, w.num_seqs, T, w.total_keys,
                                              Hq, Hkv, D, w.window, w.scale, o, l, stream)
         else:
@@ -377,7 +382,24 @@ def main():
         return 0
 
     peaks, peak_src = load_peaks()
-    achieved = flops / (attn_avg * 1e-3) / 1e12
+    if decode:
+        # A stream over the cache (about 4 FLOP per byte): the HBM roof applies.
+        achieved = w.algorithmic_bytes() / (attn_avg * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name, D),
+                    "peak_source": f"{peak_src} HBM copy bandwidth",
+                    "algorithmic_bytes": w.algorithmic_bytes(),
+                    "kernel": f"decode_split_kernel<{D}> + decode_merge_kernel<{D}>"}
+    else:
+        achieved = flops / (attn_avg * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name, D),
+                    "peak_source": f"{peak_src} dense bf16 (burst)",
+                    "algorithmic_bytes": w.algorithmic_bytes(),
+                    "kernel": ("attention_fwd_d128_kernel" if D == 128 else
+                               "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
+                               "attention_fwd_kernel<false>")}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -385,7 +407,10 @@ def main():
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, fp32 sinks)",
         "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
                    f"{len(w.seqlens)} seqs", "total_tokens": T,
-                   "key_lengths": (w.seqlens_k if kvcache else None), "Hq": Hq, "Hkv": Hkv, "D": D,
+                   "key_lengths": (w.seqlens_k if kvcache and len(w.seqlens_k) <= 8 else
+                                   (f"{len(w.seqlens_k)} seqs, {w.total_keys} keys" if kvcache
+                                    else None)),
+                   "Hq": Hq, "Hkv": Hkv, "D": D,
                    "window": w.window, "scale": w.scale, "sinks": True, "lse": True,
                    "l2": "flushed before every timed step (256 MB write)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
@@ -394,18 +419,11 @@ def main():
         "unmasked_flop_per_step": flops,
         "attention_kernel_ms": attn_avg, "prepass_kernel_ms": sum(pre_ms) / len(pre_ms),
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
-        "roofline": {"bound": "tensor", "achieved": achieved,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name, D),
-                     "peak_source": f"{peak_src} dense bf16 (burst)",
-                     "algorithmic_bytes": w.algorithmic_bytes(),
-                     "kernel": ("attention_fwd_d128_kernel" if D == 128 else
-                                "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
-                                "attention_fwd_kernel<false>")},
+        "roofline": roofline,
         "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "matches_resident_run": bool(same)},
-        "gpu_launches": args.steps * pkg.tsk_kernels_per_call(),
+        "gpu_launches": args.steps * (3 if decode else pkg.tsk_kernels_per_call()),
         "clocks": clk.summary(),
         "kernel_source_hash": kernel_source_hash(D),
     }

@@ -20,7 +20,8 @@ import os
 import threading
 
 __all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "tsk_mha_prefill_kvcache",
-           "mha_prefill", "mha_prefill_kvcache", "tsk_get_device_status", "tsk_status_string",
+           "tsk_mha_decode_kvcache", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
+           "tsk_get_device_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
            "tsk_version", "TskError", "library_path", "load_library"]
@@ -77,6 +78,9 @@ def load_library():
         lib.tsk_mha_prefill_kvcache.argtypes = [P, P, P, P, P, P, i32, i64, i64, i32, i32, i32,
                                                 i32, ctypes.c_float, P, P, P]
         lib.tsk_mha_prefill_kvcache.restype = ctypes.c_int
+        lib.tsk_mha_decode_kvcache.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32,
+                                               ctypes.c_float, P, P, P]
+        lib.tsk_mha_decode_kvcache.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
         lib.tsk_last_error.argtypes = []
@@ -161,6 +165,47 @@ def tsk_mha_prefill_kvcache(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k, num_seqs
                                        int(total_q), int(total_k), int(Hq), int(Hkv), int(D),
                                        int(window), float(scale), _ptr(out), _ptr(lse),
                                        _stream_handle(stream))
+
+
+def tsk_mha_decode_kvcache(q, k, v, sinks, cu_seqlens_k, num_seqs, total_k, max_seqlen_k, Hq,
+                           Hkv, D, window, scale, out, lse, stream=None) -> int:
+    """One decoding step over a key/value cache (same arguments as the C
+    function): the query of sequence s sits at key position Lk - 1.  Returns
+    the status code."""
+    lib = load_library()
+    return lib.tsk_mha_decode_kvcache(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens_k),
+                                      int(num_seqs), int(total_k), int(max_seqlen_k), int(Hq),
+                                      int(Hkv), int(D), int(window), float(scale), _ptr(out),
+                                      _ptr(lse), _stream_handle(stream))
+
+
+def mha_decode_kvcache(q, k, v, cu_seqlens_k, max_seqlen_k: int, sinks=None, window: int = 0,
+                       scale: float | None = None, out=None, lse=None, return_lse=True,
+                       stream=None):
+    """Tensor-level convenience over ``tsk_mha_decode_kvcache``: q [B, Hq, D],
+    k/v [Tk, Hkv, D] bf16 CUDA (D = 64 or 128), cu_seqlens_k int32 CUDA [B+1].
+    Returns (out, lse)."""
+    import torch
+    B, Hq, D = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if v.shape != k.shape or k.shape[2] != D:
+        raise ValueError("k and v must both be [Tk, Hkv, D]")
+    if cu_seqlens_k.dtype != torch.int32 or not cu_seqlens_k.is_cuda or cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_k must be an int32 CUDA tensor of B + 1 offsets")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    rc = tsk_mha_decode_kvcache(q, k, v, sinks, cu_seqlens_k, B, Tk, max_seqlen_k, Hq, Hkv, D,
+                                window, scale, out, lse if return_lse else None, stream)
+    if rc != 0:
+        raise TskError(rc, "tsk_mha_decode_kvcache")
+    return out, (lse if return_lse else None)
 
 
 def mha_prefill_kvcache(q, k, v, cu_seqlens_q, cu_seqlens_k, sinks=None, window: int = 0,

@@ -20,6 +20,7 @@ constexpr int kTileN = 128;      // keys per tile
 // Workspace words (int32) at the head of the per-stream workspace.
 constexpr int kWsStatus = 0;   // [0] error code, [1] site, [2] block
 constexpr int kWsNTiles = 4;   // number of query tiles in the list
+constexpr int kWsDecodeBad = 6;  // decode: this call's offset check
 constexpr int kWsHeader = 8;   // ints; tile offsets follow, then the int4 list (16-B aligned)
 
 // One query tile: two int4 per entry,

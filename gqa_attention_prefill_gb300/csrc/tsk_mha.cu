@@ -16,6 +16,7 @@
 #include "tsk_mha.h"
 #include "attention.cuh"
 #include "attention_d128.cuh"
+#include "decode.cuh"
 #include "schedule.cuh"
 
 namespace {
@@ -27,6 +28,8 @@ struct Workspace {
   size_t bytes = 0;
   int max_tiles = 0;
   int max_seqs = 0;
+  float* part = nullptr;  // decode: per-split partial states
+  size_t part_bytes = 0;
 };
 
 struct DeviceState {
@@ -120,6 +123,14 @@ tsk_status check_device(int* dev_out, DeviceState** st_out) {
       e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::d128::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::dec::decode_split_kernel<64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::dec::smem_bytes<64>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::dec::decode_split_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::dec::smem_bytes<128>());
     if (e != cudaSuccess) return cuda_fail(e);
     st.smem_set = true;
   }
@@ -416,11 +427,11 @@ tsk_status tsk_release(void) {
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = -1;
   if (!g_ws.empty() && cudaGetDevice(&dev) == cudaSuccess) cudaDeviceSynchronize();
-  for (auto& kv : g_ws)
-    if (kv.second.base) {
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.base);
-    }
+  for (auto& kv : g_ws) {
+    if (kv.second.base || kv.second.part) cudaSetDevice(kv.first.first);
+    if (kv.second.base) cudaFree(kv.second.base);
+    if (kv.second.part) cudaFree(kv.second.part);
+  }
   if (dev >= 0) cudaSetDevice(dev);
   g_ws.clear();
   return TSK_OK;
@@ -553,4 +564,132 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
     return TSK_ERR_LAUNCH;
   }
   return TSK_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Decode over a key/value cache (one query token per sequence).
+extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const void* v,
+                                             const float* sinks, const int32_t* cu_seqlens_k,
+                                             int32_t num_seqs, int64_t total_k,
+                                             int32_t max_seqlen_k, int32_t Hq, int32_t Hkv,
+                                             int32_t D, int32_t window, float scale, void* out,
+                                             float* lse, tsk_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!q || !k || !v || !out || !cu_seqlens_k) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_k < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (max_seqlen_k < 1 || (int64_t)max_seqlen_k > total_k ||
+                       total_k < (int64_t)num_seqs))
+    return TSK_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || total_k * (int64_t)Hkv >= ((int64_t)1 << 31) ||
+      (int64_t)num_seqs * Hq >= ((int64_t)1 << 31))
+    return TSK_ERR_UNSUPPORTED;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
+  if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return TSK_ERR_ALIGNMENT;
+  if (!a4(cu_seqlens_k) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
+  const size_t qo_bytes = (size_t)num_seqs * Hq * D * 2;
+  const size_t kv_bytes = (size_t)total_k * Hkv * D * 2;
+  if (num_seqs > 0 && (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k, kv_bytes) ||
+                       overlaps(out, qo_bytes, v, kv_bytes)))
+    return TSK_ERR_INVALID_ARG;
+  if (num_seqs == 0) return TSK_OK;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  DeviceState* ds = nullptr;
+  tsk_status st = check_device(&dev, &ds);
+  if (st != TSK_OK) return st;
+  if ((st = get_encoder()) != TSK_OK) return st;
+  Workspace* ws = nullptr;
+  if ((st = get_workspace(dev, stream, 1024, 1024, &ws)) != TSK_OK) return st;
+
+  // Key splits: enough CTAs for about two waves at the kernel's occupancy.
+  const int G = Hq / Hkv;
+  const int n_hb = (G + tsk::dec::kRows - 1) / tsk::dec::kRows;
+  const int span = window > 0 && window < max_seqlen_k ? window : max_seqlen_k;
+  const int n_tiles = (span + tsk::dec::kKeys - 1) / tsk::dec::kKeys;
+  const int64_t base_ctas = (int64_t)num_seqs * Hkv * n_hb;
+  const int64_t target = (int64_t)ds->num_sms * (D == 64 ? 4 : 2);
+  int splits = (int)((target + base_ctas - 1) / base_ctas);
+  splits = splits < 1 ? 1 : (splits > n_tiles ? n_tiles : splits);
+  const int tps = (n_tiles + splits - 1) / splits;
+  splits = (n_tiles + tps - 1) / tps;
+
+  const size_t need = (size_t)splits * num_seqs * Hq * (D + 2) * sizeof(float);
+  if (ws->part_bytes < need) {
+    float* nb = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), need, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode workspace");
+    if (ws->part) cudaFreeAsync(ws->part, stream);
+    ws->part = nb;
+    ws->part_bytes = need;
+  }
+
+  CUtensorMap tk, tv;
+  if ((st = encode_thd(&tk, k, total_k, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, total_k, Hkv, D)) != TSK_OK) return st;
+
+  tsk::dec::DecParams p;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  p.sinks = sinks;
+  p.cu_k = cu_seqlens_k;
+  p.part = ws->part;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = ws->base + tsk::kWsStatus;
+  p.bad = ws->base + tsk::kWsDecodeBad;
+  p.num_seqs = num_seqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.n_hb = n_hb;
+  p.window = window;
+  p.splits = splits;
+  p.tiles_per_split = tps;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+
+  char name[160];
+  snprintf(name, sizeof name, "tsk_mha_decode_kvcache[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,Tk=%lld,splits=%d]",
+           Hq, Hkv, D, window, num_seqs, (long long)total_k, splits);
+  nvtxRangePushA(name);
+  const bool prof = g_profile;
+  if (prof) {
+    if (g_ev_dev != dev) {
+      for (auto& e : g_ev) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
+      }
+      for (auto& e : g_ev)
+        if (cudaEventCreate(&e) != cudaSuccess) {
+          nvtxRangePop();
+          return TSK_ERR_DEVICE;
+        }
+      g_ev_dev = dev;
+    }
+    cudaEventRecord(g_ev[0], stream);
+  }
+  tsk::dec::decode_check_kernel<<<1, 1024, 0, stream>>>(cu_seqlens_k, num_seqs, (int)total_k,
+                                                       max_seqlen_k, ws->base + tsk::kWsStatus,
+                                                       ws->base + tsk::kWsDecodeBad);
+  if (prof) cudaEventRecord(g_ev[1], stream);
+  const dim3 grid(splits, Hkv * n_hb, num_seqs);
+  const int mgrid = (int)(((int64_t)num_seqs * Hq * 32 + 255) / 256);
+  if (D == 64) {
+    tsk::dec::decode_split_kernel<64><<<grid, tsk::dec::kThreads, tsk::dec::smem_bytes<64>(), stream>>>(tk, tv, p);
+    tsk::dec::decode_merge_kernel<64><<<mgrid, 256, 0, stream>>>(p);
+  } else {
+    tsk::dec::decode_split_kernel<128><<<grid, tsk::dec::kThreads, tsk::dec::smem_bytes<128>(), stream>>>(tk, tv, p);
+    tsk::dec::decode_merge_kernel<128><<<mgrid, 256, 0, stream>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) note_error("decode kernel launch", e);
+  if (prof) {
+    cudaEventRecord(g_ev[2], stream);
+    g_ev_recorded = true;
+  }
+  nvtxRangePop();
+  return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
 }

@@ -115,6 +115,39 @@ TSK_API tsk_status tsk_mha_prefill_kvcache(const void *q, const void *k, const v
                                            int32_t Hkv, int32_t D, int32_t window, float scale,
                                            void *out, float *lse, tsk_stream_t stream);
 
+/*
+ * tsk_mha_decode_kvcache -- one decoding step over a key/value cache (README,
+ * section "Public API": the decode call of the same runtime path; the pages
+ * give no formula).  Sequence s has one new query token q[s] and
+ * Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s] >= 1 keys/values whose last one is
+ * the token's own; the token sits at key position Lk - 1 and attends to key
+ * positions max(0, Lk - W) .. Lk - 1 (all of them for W <= 0), with the sink
+ * of its head counted once.  Identical to tsk_mha_prefill_kvcache with one
+ * query per sequence.  The keys of a sequence are split over several CTAs
+ * when the batch alone would not fill the GPU; the splits' partial softmax
+ * states are merged by a second kernel.
+ *
+ *   q             device, bf16 [num_seqs, Hq, D]
+ *   k, v          device, bf16 [total_k, Hkv, D] (contiguous per sequence)
+ *   sinks         device, fp32 [Hq] or NULL
+ *   cu_seqlens_k  device, int32 [num_seqs + 1]: 0 = cu[0] < cu[1] < ... = total_k
+ *   max_seqlen_k  host: an upper bound of every Lk (sizes the key splits);
+ *                 1 <= max_seqlen_k <= total_k
+ *   D             64 or 128; Hq % Hkv == 0 (any group size)
+ *   out           device, bf16 [num_seqs, Hq, D]; lse fp32 [num_seqs, Hq] or NULL
+ *
+ * Offsets that are not strictly increasing, do not end at total_k or have a
+ * length above max_seqlen_k are reported as TSK_ERR_BAD_SEQLENS through
+ * tsk_get_device_status and nothing is written.  Limits: num_seqs <= 65535,
+ * total_k * Hkv < 2^31.  The library keeps a per-(device, stream) buffer of
+ * splits x num_seqs x Hq x (D + 2) floats for the partial states.
+ */
+TSK_API tsk_status tsk_mha_decode_kvcache(const void *q, const void *k, const void *v,
+                                         const float *sinks, const int32_t *cu_seqlens_k,
+                                         int32_t num_seqs, int64_t total_k, int32_t max_seqlen_k,
+                                         int32_t Hq, int32_t Hkv, int32_t D, int32_t window,
+                                         float scale, void *out, float *lse, tsk_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 TSK_API const char *tsk_status_string(tsk_status s);
 

@@ -203,6 +203,11 @@ CONFIGS = {
     # prefill over a key/value cache (not one of the five above)
     "kvcache_4x2048_on_4096_h64kv8": dict(desc="4 seqs x 2048 new tokens over a 4096-token cache "
                                                "(Lk = 6144), Hq=64, Hkv=8, D=64, causal"),
+    # one decoding step per sequence over its cache (query at key position Lk - 1)
+    "decode_64x8192_h64kv8": dict(desc="64 seqs, one query token each over 8192 keys, Hq=64, "
+                                       "Hkv=8, D=64, sinks N(0,1), causal"),
+    "decode_ragged32_h64kv8": dict(desc="32 seqs, one query token each over U{512..32768} keys, "
+                                        "Hq=64, Hkv=8, D=64, sinks N(0,2), causal"),
     # head dimension 128 (the same unmasked FLOPs as causal_4x4096_h64kv8)
     "causal_4x4096_h32kv8_d128": dict(desc="4 seqs x 4096 tokens, Hq=32, Hkv=8, D=128, "
                                            "sinks N(0,1), scale 1/sqrt(128), full causal"),
@@ -230,6 +235,11 @@ def config(name: str, seed: int = 0) -> Workload:
         return make([32768], 64, 8, k_mult=3.0, seed=seed, name=name)
     if name == "kvcache_4x2048_on_4096_h64kv8":
         return make_kvcache([2048] * 4, [6144] * 4, 64, 8, seed=seed, name=name)
+    if name == "decode_64x8192_h64kv8":
+        return make_kvcache([1] * 64, [8192] * 64, 64, 8, seed=seed, name=name)
+    if name == "decode_ragged32_h64kv8":
+        return make_kvcache([1] * 32, ragged_lengths(seed, 32, 512, 32768), 64, 8, sink_sigma=2.0,
+                            seed=seed, name=name)
     if name == "causal_4x4096_h32kv8_d128":
         return make([4096] * 4, 32, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
     if name == "long_1x32768_h32kv8_d128":

@@ -115,3 +115,26 @@ def test_kvcache_host_side_rejections(lib, kw, code):
 
 def test_kvcache_empty_returns_ok(lib):
     assert kv_call(lib, total_q=0, total_k=0) == 0
+
+
+def dec_call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 3, v=FAKE * 5, sinks=None, cu_k=FAKE * 13, num_seqs=4, total_k=512,
+             max_k=256, Hq=8, Hkv=2, D=64, window=0, scale=0.125, out=FAKE * 9, lse=None)
+    a.update(kw)
+    return lib.tsk_mha_decode_kvcache(a["q"], a["k"], a["v"], a["sinks"], a["cu_k"], a["num_seqs"],
+                                      a["total_k"], a["max_k"], a["Hq"], a["Hkv"], a["D"],
+                                      a["window"], a["scale"], a["out"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_k=None), -1), (dict(q=None), -1), (dict(max_k=0), -1), (dict(max_k=1000), -1),
+    (dict(total_k=2), -1), (dict(scale=0.0), -1), (dict(D=96), -2), (dict(Hq=6, Hkv=4), -2),
+    (dict(num_seqs=70000, total_k=1 << 20, max_k=64), -2), (dict(q=FAKE + 8), -3),
+    (dict(cu_k=FAKE * 13 + 2), -3), (dict(out=FAKE * 3 + 16), -1),
+])
+def test_decode_host_side_rejections(lib, kw, code):
+    assert dec_call(lib, **kw) == code
+
+
+def test_decode_empty_returns_ok(lib):
+    assert dec_call(lib, num_seqs=0, total_k=0) == 0
