@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "tsk_mha_prefill_kvcache",
-           "tsk_mha_decode_kvcache", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
+           "tsk_mha_decode_kvcache", "tsk_mha_prefill_paged", "tsk_mha_decode_paged", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
            "tsk_get_device_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
@@ -81,6 +81,12 @@ def load_library():
         lib.tsk_mha_decode_kvcache.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32,
                                                ctypes.c_float, P, P, P]
         lib.tsk_mha_decode_kvcache.restype = ctypes.c_int
+        lib.tsk_mha_prefill_paged.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i64, i64,
+                                              i32, i32, i32, i32, ctypes.c_float, P, P, P]
+        lib.tsk_mha_prefill_paged.restype = ctypes.c_int
+        lib.tsk_mha_decode_paged.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i32, i32,
+                                             i32, i32, i32, ctypes.c_float, P, P, P]
+        lib.tsk_mha_decode_paged.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
         lib.tsk_last_error.argtypes = []
@@ -177,6 +183,33 @@ def tsk_mha_decode_kvcache(q, k, v, sinks, cu_seqlens_k, num_seqs, total_k, max_
                                       int(num_seqs), int(total_k), int(max_seqlen_k), int(Hq),
                                       int(Hkv), int(D), int(window), float(scale), _ptr(out),
                                       _ptr(lse), _stream_handle(stream))
+
+
+def tsk_mha_prefill_paged(q, k_pages, v_pages, sinks, cu_seqlens_q, cu_seqlens_k, block_table,
+                          max_blocks_per_seq, page_size, num_pages, num_seqs, total_q, total_k,
+                          Hq, Hkv, D, window, scale, out, lse, stream=None) -> int:
+    """Prefill over a paged key/value cache (same arguments as the C
+    function).  Returns the status code."""
+    lib = load_library()
+    return lib.tsk_mha_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(sinks),
+                                     _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(block_table),
+                                     int(max_blocks_per_seq), int(page_size), int(num_pages),
+                                     int(num_seqs), int(total_q), int(total_k), int(Hq), int(Hkv),
+                                     int(D), int(window), float(scale), _ptr(out), _ptr(lse),
+                                     _stream_handle(stream))
+
+
+def tsk_mha_decode_paged(q, k_pages, v_pages, sinks, cu_seqlens_k, block_table, max_blocks_per_seq,
+                         page_size, num_pages, num_seqs, total_k, max_seqlen_k, Hq, Hkv, D, window,
+                         scale, out, lse, stream=None) -> int:
+    """One decoding step over a paged key/value cache (same arguments as the C
+    function).  Returns the status code."""
+    lib = load_library()
+    return lib.tsk_mha_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(sinks),
+                                    _ptr(cu_seqlens_k), _ptr(block_table), int(max_blocks_per_seq),
+                                    int(page_size), int(num_pages), int(num_seqs), int(total_k),
+                                    int(max_seqlen_k), int(Hq), int(Hkv), int(D), int(window),
+                                    float(scale), _ptr(out), _ptr(lse), _stream_handle(stream))
 
 
 def mha_decode_kvcache(q, k, v, cu_seqlens_k, max_seqlen_k: int, sinks=None, window: int = 0,

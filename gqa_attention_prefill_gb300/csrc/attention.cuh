@@ -76,6 +76,7 @@ struct AttnParams {
   float scale_log2;     // scale * log2(e)
   unsigned long long timeout_ns;
   int debug_stall;      // test hook: producer first waits on a barrier nothing signals
+  PagedKV kv;           // paged key/value cache, or kv.page_size == 0 (contiguous)
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.
@@ -106,8 +107,9 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, in
 
 struct Unit {
   int start, q0, kv_lo, len, n_kv, g, h0, ntiles;
-  int start_k;  // first key row of the sequence
+  int start_k;  // first key row of the sequence (contiguous cache)
   int offset;   // Lk - Lq: key position of query row 0
+  int seq;      // sequence index (block-table row of a paged cache)
 };
 
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
@@ -124,6 +126,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   r.start_k = f.x;
   r.offset = f.y;
   r.n_kv = f.z;
+  r.seq = f.w;
   r.g = rem / p.HP;
   const int hp = rem - r.g * p.HP;
   r.h0 = r.g * p.G + 2 * hp;
@@ -141,6 +144,36 @@ __device__ __forceinline__ int4 ld_nc_v4_volatile(const int4* a) {
   return v;
 }
 
+
+// TMA loads of the 128 cache rows holding key positions pos0 .. pos0 + 127 of
+// sequence `seq` (Lk keys) from a paged cache into the 128-byte rows at `dst`,
+// x = first of the 64 columns: one box per page chunk (min(page_size, 128)
+// rows, at least 8: chunks start on 1024-byte boundaries, so the 128-byte
+// swizzle is that of a single box); chunks past the sequence's last page
+// re-read that page (their keys are masked).  Out of line: it is rare next to
+// the contiguous case and stays out of the kernels' hot code.
+__device__ __noinline__ void tma_load_key_rows_paged(uint32_t dst, const CUtensorMap* tm,
+                                                     uint32_t bar, int x, int head,
+                                                     const PagedKV pg, int seq, int pos0, int Lk) {
+  const int chunk = pg.page_size < 128 ? pg.page_size : 128;
+  const int last_blk = (Lk - 1) / pg.page_size;
+  for (int c = 0; c < 128; c += chunk) {
+    const int pos = pos0 + c;
+    int blk = pos / pg.page_size;
+    if (blk > last_blk) blk = last_blk;
+    const int page = __ldg(pg.table + (size_t)seq * pg.max_blocks + blk);
+    tma_load_3d(dst + (uint32_t)c * 128u, tm, bar, x, head, page * pg.page_size + pos % pg.page_size);
+  }
+}
+
+// The same for either cache layout; a contiguous cache (page_size 0) is one
+// box at row row0 + pos0.
+__device__ __forceinline__ void tma_load_key_rows(uint32_t dst, const CUtensorMap* tm,
+                                                  uint32_t bar, int x, int head, const PagedKV& pg,
+                                                  int seq, int row0, int pos0, int Lk) {
+  if (pg.page_size == 0) tma_load_3d(dst, tm, bar, x, head, row0 + pos0);
+  else tma_load_key_rows_paged(dst, tm, bar, x, head, pg, seq, pos0, Lk);
+}
 
 // State shared by the roles of one CTA.
 struct Ctx {
@@ -176,12 +209,14 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
       const uint32_t k = kv_iter / kStages;
       if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, 2, p, cx.abort);
       if (!ok) break;
-      const int row = w.start_k + (w.kv_lo + j) * kTileN;
+      const int pos0 = (w.kv_lo + j) * kTileN;  // key position of the tile's first key
+      const int Lk = w.offset + w.len;
       const uint32_t kdst = cx.sbase + kSmemKV + s * 2 * kTileBytes;
       mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTileBytes);
-      tma_load_3d(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, row);
+      tma_load_key_rows(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, p.kv, w.seq, w.start_k, pos0, Lk);
       mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kTileBytes);
-      tma_load_3d(kdst + kTileBytes, tmV, cx.bar(kBarVFull + s), 0, w.g, row);
+      tma_load_key_rows(kdst + kTileBytes, tmV, cx.bar(kBarVFull + s), 0, w.g, p.kv, w.seq,
+                        w.start_k, pos0, Lk);
     }
   }
   // Drain: wait for the last load issued into every buffer so that no

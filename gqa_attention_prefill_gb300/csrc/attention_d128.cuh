@@ -93,7 +93,8 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     TSK_EV(20);
     ++q_iter;
     for (int j = 0; j < w.n_kv && ok; ++j) {
-      const int row = w.start_k + (w.kv_lo + j) * kTileN;
+      const int pos0 = (w.kv_lo + j) * kTileN;  // key position of the tile's first key
+      const int Lk = w.offset + w.len;
       {
         const int s = k_iss % kStagesKV;
         const uint32_t k = k_iss / kStagesKV;
@@ -102,7 +103,8 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
         const uint32_t dst = cx.sbase + kSmemKV + s * 2 * kTile;
         mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTile);
         for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g, row);
+          tma_load_key_rows(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g, p.kv,
+                            w.seq, w.start_k, pos0, Lk);
         TSK_EV(21);
         ++k_iss;
       }
@@ -114,7 +116,8 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
         const uint32_t dst = cx.sbase + kSmemKV + s * 2 * kTile + kTile;
         mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kTile);
         for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g, row);
+          tma_load_key_rows(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g, p.kv,
+                            w.seq, w.start_k, pos0, Lk);
         TSK_EV(22);
         ++v_iss;
       }

@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "attention.cuh"
 
 namespace tsk {
 namespace dec {
@@ -45,6 +46,7 @@ struct DecParams {
   int splits, tiles_per_split;
   float scale_log2;         // scale * log2(e)
   unsigned long long timeout_ns;
+  PagedKV kv;               // paged key/value cache, or kv.page_size == 0 (contiguous)
 };
 
 template <int D>
@@ -92,11 +94,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
 // cu_k[num_seqs] = total_k.  Writes this call's verdict to *bad and, on
 // failure, TSK_ERR_BAD_SEQLENS (-8) to the sticky status word.
 __global__ void decode_check_kernel(const int* cu_k, int num_seqs, int total_k, int max_k,
-                                    int* status, int* bad_out) {
+                                    int* status, int* bad_out, PagedKV pg) {
   bool bad = false;
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
     const int a = cu_k[s], b = cu_k[s + 1];
     if (a < 0 || b < a + 1 || b - a > max_k || b > total_k) bad = true;
+    else if (!pages_ok(pg, s, b - a)) bad = true;
   }
   if (threadIdx.x == 0 && (cu_k[0] != 0 || cu_k[num_seqs] != total_k)) bad = true;
   bad = __syncthreads_or(bad);
@@ -131,8 +134,9 @@ __global__ void __launch_bounds__(kThreads)
 
   const int k0 = p.cu_k[b], Lk = p.cu_k[b + 1] - k0;
   const int lo = p.window > 0 ? max(0, Lk - p.window) : 0;  // first visible key position
+  const int lo_al = lo - lo % kKeys;  // tiles start on multiples of 128 key positions
   const int t_begin = split * p.tiles_per_split;
-  const int n_tiles_seq = (Lk - lo + kKeys - 1) / kKeys;
+  const int n_tiles_seq = (Lk - lo_al + kKeys - 1) / kKeys;
   const int t_end = min(n_tiles_seq, t_begin + p.tiles_per_split);
   const int nt = max(0, t_end - t_begin);  // tiles of this CTA
   const int h_lo = hb * kRows;             // first query head of the block within the group
@@ -157,12 +161,14 @@ __global__ void __launch_bounds__(kThreads)
     if (i >= kStages) ok = ok && mbar_wait(bar_empty + 8 * s, ((i / kStages) - 1) & 1, 30, pw, abort_addr);
     if (!ok) return;
     issued = i + 1;
-    const int row = k0 + lo + (t_begin + i) * kKeys;
+    const int pos0 = lo_al + (t_begin + i) * kKeys;
     const uint32_t dst = sbase + (uint32_t)s * 2u * kTile;
     mbar_arrive_expect_tx(bar_full + 8 * s, 2 * kTile);
     for (int hf = 0; hf < D / 64; ++hf) {
-      tma_load_3d(dst + hf * (kKeys * 128), &tmK, bar_full + 8 * s, 64 * hf, g, row);
-      tma_load_3d(dst + kTile + hf * (kKeys * 128), &tmV, bar_full + 8 * s, 64 * hf, g, row);
+      tma_load_key_rows(dst + hf * (kKeys * 128), &tmK, bar_full + 8 * s, 64 * hf, g, p.kv, b, k0,
+                        pos0, Lk);
+      tma_load_key_rows(dst + kTile + hf * (kKeys * 128), &tmV, bar_full + 8 * s, 64 * hf, g, p.kv,
+                        b, k0, pos0, Lk);
     }
   };
   if (threadIdx.x == 0)
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kThreads)
     ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_full + 8 * s, (i / kStages) & 1, 31, pw, abort_addr));
     if (!ok) break;
     const uint32_t kt = sbase + (uint32_t)s * 2u * kTile, vt = kt + kTile;
-    const int key0 = lo + (t_begin + i) * kKeys + 32 * warp;  // key position of the warp's first key
+    const int key0 = lo_al + (t_begin + i) * kKeys + 32 * warp;  // key position of the warp's first key
 
     // S (16 x 32) = Q K^T for the warp's 32 keys.
     float sc[4][4];
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int kp = key0 + 8 * n + (lane & 3) * 2 + e;
-        const bool in = kp < Lk;
+        const bool in = kp < Lk && kp >= lo;
         sc[n][e] = in ? sc[n][e] * sl2 : -INFINITY;
         sc[n][2 + e] = in ? sc[n][2 + e] * sl2 : -INFINITY;
         mt0 = fmaxf(mt0, sc[n][e]);

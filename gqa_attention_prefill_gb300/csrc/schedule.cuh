@@ -41,11 +41,32 @@ __device__ __forceinline__ int2 qtile_key_range(int q0, int len_q, int offset, i
   return make_int2(kv_lo, kv_hi - kv_lo + 1);
 }
 
+// Paged key/value cache (page_size > 0): sequence s's key position x lives in
+// page block_table[s * max_blocks + x / page_size], slot x % page_size.
+struct PagedKV {
+  const int32_t* table;
+  int max_blocks;
+  int page_size;  // 0: contiguous cache
+  int num_pages;
+};
+
+// True when sequence s (Lk keys) has a valid page for every key.
+__device__ __forceinline__ bool pages_ok(const PagedKV& pg, int s, int Lk) {
+  if (pg.page_size == 0) return true;
+  const int nb = (Lk + pg.page_size - 1) / pg.page_size;
+  if (nb > pg.max_blocks) return false;
+  for (int i = 0; i < nb; ++i) {
+    const int pgi = pg.table[(size_t)s * pg.max_blocks + i];
+    if (pgi < 0 || pgi >= pg.num_pages) return false;
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k,
                     int num_seqs, int total_tokens, int total_keys, int window,
                     int* __restrict__ ws, int* __restrict__ tile_off, int4* __restrict__ list,
-                    int max_tiles) {
+                    int max_tiles, PagedKV pg) {
   __shared__ int s_scan[kSchedThreads];
   __shared__ int s_hist[kCostBins];
   __shared__ int s_cursor[kCostBins];
@@ -69,7 +90,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     if (s < num_seqs) {
       int L = cu[s + 1] - cu[s];
       const int Lk = cu_k[s + 1] - cu_k[s];
-      if (L < 0 || Lk < L) {
+      if (L < 0 || Lk < L || !pages_ok(pg, s, Lk)) {
         s_bad = 1;
         L = 0;
       }
@@ -154,7 +175,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     const int2 kr = qtile_key_range(q0, len, offset, window);
     const int pos = atomicAdd(&s_cursor[min(kr.y, kCostBins) - 1], 1);
     list[2 * pos] = make_int4(cu[s], q0, kr.x, len);
-    list[2 * pos + 1] = make_int4(cu_k[s], offset, kr.y, 0);
+    list[2 * pos + 1] = make_int4(cu_k[s], offset, kr.y, s);
   }
   if (tid == 0) ws[kWsNTiles] = n_tiles;
 }

@@ -259,11 +259,25 @@ void launch_attention(int D, int window, int grid, const CUtensorMap& tq, const 
 
 // Shared by tsk_mha_prefill (cu_k == cu_q, total_keys == total_queries) and
 // tsk_mha_prefill_kvcache.
+// Host checks of a paged cache description; rows = cache rows it spans.
+tsk_status check_paged(const int32_t* table, int32_t max_blocks, int32_t page_size,
+                       int32_t num_pages, int32_t num_seqs, int32_t Hkv, int64_t* rows) {
+  if (!table || max_blocks < 1 || num_pages < 1) return TSK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(table) & 3) != 0) return TSK_ERR_ALIGNMENT;
+  if (page_size < 8 || page_size % 8 != 0 || (page_size % 128 != 0 && 128 % page_size != 0))
+    return TSK_ERR_UNSUPPORTED;
+  *rows = (int64_t)num_pages * page_size;
+  if (*rows * Hkv >= ((int64_t)1 << 31) || (int64_t)num_seqs * max_blocks >= ((int64_t)1 << 31))
+    return TSK_ERR_UNSUPPORTED;
+  return TSK_OK;
+}
+
 tsk_status prefill_impl(const void* q, const void* k, const void* v, const float* sinks,
                         const int32_t* cu_q, const int32_t* cu_k, int32_t num_seqs,
                         int64_t total_q, int64_t total_k, int32_t Hq, int32_t Hkv, int32_t D,
                         int32_t window, float scale, void* out, float* lse,
-                        cudaStream_t stream, const char* what) {
+                        cudaStream_t stream, const char* what, const int32_t* block_table = nullptr,
+                        int32_t max_blocks = 0, int32_t page_size = 0, int32_t num_pages = 0) {
   // ---- host-only checks (no CUDA call before these pass)
   if (!q || !k || !v || !out || !cu_q || !cu_k) return TSK_ERR_INVALID_ARG;
   if (num_seqs < 0 || total_q < 0 || total_k < 0 || Hq <= 0 || Hkv <= 0)
@@ -279,12 +293,19 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return TSK_ERR_ALIGNMENT;
   if (!a4(cu_q) || !a4(cu_k) || (sinks && !a4(sinks)) || (lse && !a4(lse)))
     return TSK_ERR_ALIGNMENT;
+  int64_t kv_rows = total_k;  // rows of the k and v buffers
+  if (page_size != 0) {
+    tsk_status pst = check_paged(block_table, max_blocks, page_size, num_pages, num_seqs, Hkv, &kv_rows);
+    if (pst != TSK_OK) return pst;
+  }
   const size_t qo_bytes = (size_t)total_q * Hq * D * 2;
-  const size_t kv_bytes = (size_t)total_k * Hkv * D * 2;
+  const size_t kv_bytes = (size_t)kv_rows * Hkv * D * 2;
   if (total_q > 0 && (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k, kv_bytes) ||
                       overlaps(out, qo_bytes, v, kv_bytes)))
     return TSK_ERR_INVALID_ARG;
   if (num_seqs == 0 || total_q == 0) return TSK_OK;
+  const tsk::PagedKV pg{block_table, max_blocks, page_size, num_pages};
+  const int kv_box = page_size != 0 && page_size < 128 ? page_size : 128;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = -1;
@@ -300,8 +321,8 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
 
   CUtensorMap tq, tk, tv, to;
   if ((st = encode_thd(&tq, q, total_q, Hq, D)) != TSK_OK) return st;
-  if ((st = encode_thd(&tk, k, total_k, Hkv, D)) != TSK_OK) return st;
-  if ((st = encode_thd(&tv, v, total_k, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, kv_rows, Hkv, D, kv_box)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, kv_rows, Hkv, D, kv_box)) != TSK_OK) return st;
   if ((st = encode_thd(&to, out, total_q, Hq, D, 32)) != TSK_OK) return st;
 
   char name[112];
@@ -331,7 +352,7 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   }
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
       cu_q, cu_k, num_seqs, (int)total_q, (int)total_k, window, ws->base, tile_off, list,
-      ws->max_tiles);
+      ws->max_tiles, pg);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
   tsk::AttnParams p;
@@ -349,6 +370,7 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = g_debug_stall;
+  p.kv = pg;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   launch_attention(D, window, grid, tq, tk, tv, to, p, stream);
@@ -384,6 +406,20 @@ tsk_status tsk_mha_prefill_kvcache(const void* q, const void* k, const void* v,
   return prefill_impl(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
                       Hq, Hkv, D, window, scale, out, lse,
                       reinterpret_cast<cudaStream_t>(stream), "tsk_mha_prefill_kvcache");
+}
+
+tsk_status tsk_mha_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const float* sinks, const int32_t* cu_seqlens_q,
+                                 const int32_t* cu_seqlens_k, const int32_t* block_table,
+                                 int32_t max_blocks_per_seq, int32_t page_size, int32_t num_pages,
+                                 int32_t num_seqs, int64_t total_q, int64_t total_k, int32_t Hq,
+                                 int32_t Hkv, int32_t D, int32_t window, float scale, void* out,
+                                 float* lse, tsk_stream_t stream) {
+  if (page_size == 0) return TSK_ERR_UNSUPPORTED;
+  return prefill_impl(q, k_pages, v_pages, sinks, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
+                      total_k, Hq, Hkv, D, window, scale, out, lse,
+                      reinterpret_cast<cudaStream_t>(stream), "tsk_mha_prefill_paged",
+                      block_table, max_blocks_per_seq, page_size, num_pages);
 }
 
 tsk_status tsk_get_device_status(tsk_stream_t stream_) {
@@ -538,7 +574,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch header");
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, scratch,
-      tile_off, list, kNoAllocMaxTiles);
+      tile_off, list, kNoAllocMaxTiles, tsk::PagedKV{nullptr, 0, 0, 0});
 
   tsk::AttnParams p;
   p.sinks = sinks;
@@ -555,6 +591,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = 0;
+  p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   launch_attention(D, window, grid, tq, tk, tv, to, p, stream);
@@ -568,13 +605,13 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
 
 // ---------------------------------------------------------------------------
 // Decode over a key/value cache (one query token per sequence).
-extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const void* v,
-                                             const float* sinks, const int32_t* cu_seqlens_k,
-                                             int32_t num_seqs, int64_t total_k,
-                                             int32_t max_seqlen_k, int32_t Hq, int32_t Hkv,
-                                             int32_t D, int32_t window, float scale, void* out,
-                                             float* lse, tsk_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+namespace {
+tsk_status decode_impl(const void* q, const void* k, const void* v, const float* sinks,
+                       const int32_t* cu_seqlens_k, int32_t num_seqs, int64_t total_k,
+                       int32_t max_seqlen_k, int32_t Hq, int32_t Hkv, int32_t D, int32_t window,
+                       float scale, void* out, float* lse, cudaStream_t stream, const char* what,
+                       const int32_t* block_table, int32_t max_blocks, int32_t page_size,
+                       int32_t num_pages) {
   if (!q || !k || !v || !out || !cu_seqlens_k) return TSK_ERR_INVALID_ARG;
   if (num_seqs < 0 || total_k < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
@@ -589,12 +626,19 @@ extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const
   auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
   if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return TSK_ERR_ALIGNMENT;
   if (!a4(cu_seqlens_k) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
+  int64_t kv_rows = total_k;
+  if (page_size != 0) {
+    tsk_status pst = check_paged(block_table, max_blocks, page_size, num_pages, num_seqs, Hkv, &kv_rows);
+    if (pst != TSK_OK) return pst;
+  }
   const size_t qo_bytes = (size_t)num_seqs * Hq * D * 2;
-  const size_t kv_bytes = (size_t)total_k * Hkv * D * 2;
+  const size_t kv_bytes = (size_t)kv_rows * Hkv * D * 2;
   if (num_seqs > 0 && (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k, kv_bytes) ||
                        overlaps(out, qo_bytes, v, kv_bytes)))
     return TSK_ERR_INVALID_ARG;
   if (num_seqs == 0) return TSK_OK;
+  const tsk::PagedKV pg{block_table, max_blocks, page_size, num_pages};
+  const int kv_box = page_size != 0 && page_size < 128 ? page_size : 128;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = -1;
@@ -608,8 +652,11 @@ extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const
   // Key splits: enough CTAs for about two waves at the kernel's occupancy.
   const int G = Hq / Hkv;
   const int n_hb = (G + tsk::dec::kRows - 1) / tsk::dec::kRows;
-  const int span = window > 0 && window < max_seqlen_k ? window : max_seqlen_k;
-  const int n_tiles = (span + tsk::dec::kKeys - 1) / tsk::dec::kKeys;
+  // Tiles start at multiples of 128 key positions, so a window's span can
+  // touch one tile more than its length needs.
+  const bool windowed = window > 0 && window < max_seqlen_k;
+  const int span = windowed ? window : max_seqlen_k;
+  const int n_tiles = (span + tsk::dec::kKeys - 1) / tsk::dec::kKeys + (windowed ? 1 : 0);
   const int64_t base_ctas = (int64_t)num_seqs * Hkv * n_hb;
   const int64_t target = (int64_t)ds->num_sms * (D == 64 ? 4 : 2);
   int splits = (int)((target + base_ctas - 1) / base_ctas);
@@ -628,8 +675,8 @@ extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const
   }
 
   CUtensorMap tk, tv;
-  if ((st = encode_thd(&tk, k, total_k, Hkv, D)) != TSK_OK) return st;
-  if ((st = encode_thd(&tv, v, total_k, Hkv, D)) != TSK_OK) return st;
+  if ((st = encode_thd(&tk, k, kv_rows, Hkv, D, kv_box)) != TSK_OK) return st;
+  if ((st = encode_thd(&tv, v, kv_rows, Hkv, D, kv_box)) != TSK_OK) return st;
 
   tsk::dec::DecParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(q);
@@ -650,10 +697,11 @@ extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const
   p.tiles_per_split = tps;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
+  p.kv = pg;
 
   char name[160];
-  snprintf(name, sizeof name, "tsk_mha_decode_kvcache[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,Tk=%lld,splits=%d]",
-           Hq, Hkv, D, window, num_seqs, (long long)total_k, splits);
+  snprintf(name, sizeof name, "%s[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,Tk=%lld,splits=%d]", what, Hq,
+           Hkv, D, window, num_seqs, (long long)total_k, splits);
   nvtxRangePushA(name);
   const bool prof = g_profile;
   if (prof) {
@@ -673,7 +721,7 @@ extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const
   }
   tsk::dec::decode_check_kernel<<<1, 1024, 0, stream>>>(cu_seqlens_k, num_seqs, (int)total_k,
                                                        max_seqlen_k, ws->base + tsk::kWsStatus,
-                                                       ws->base + tsk::kWsDecodeBad);
+                                                       ws->base + tsk::kWsDecodeBad, pg);
   if (prof) cudaEventRecord(g_ev[1], stream);
   const dim3 grid(splits, Hkv * n_hb, num_seqs);
   const int mgrid = (int)(((int64_t)num_seqs * Hq * 32 + 255) / 256);
@@ -692,4 +740,29 @@ extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const
   }
   nvtxRangePop();
   return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
+}
+}  // namespace
+
+extern "C" tsk_status tsk_mha_decode_kvcache(const void* q, const void* k, const void* v,
+                                             const float* sinks, const int32_t* cu_seqlens_k,
+                                             int32_t num_seqs, int64_t total_k,
+                                             int32_t max_seqlen_k, int32_t Hq, int32_t Hkv,
+                                             int32_t D, int32_t window, float scale, void* out,
+                                             float* lse, tsk_stream_t stream) {
+  return decode_impl(q, k, v, sinks, cu_seqlens_k, num_seqs, total_k, max_seqlen_k, Hq, Hkv, D,
+                     window, scale, out, lse, reinterpret_cast<cudaStream_t>(stream),
+                     "tsk_mha_decode_kvcache", nullptr, 0, 0, 0);
+}
+
+extern "C" tsk_status tsk_mha_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                           const float* sinks, const int32_t* cu_seqlens_k,
+                                           const int32_t* block_table, int32_t max_blocks_per_seq,
+                                           int32_t page_size, int32_t num_pages, int32_t num_seqs,
+                                           int64_t total_k, int32_t max_seqlen_k, int32_t Hq,
+                                           int32_t Hkv, int32_t D, int32_t window, float scale,
+                                           void* out, float* lse, tsk_stream_t stream) {
+  if (page_size == 0) return TSK_ERR_UNSUPPORTED;
+  return decode_impl(q, k_pages, v_pages, sinks, cu_seqlens_k, num_seqs, total_k, max_seqlen_k,
+                     Hq, Hkv, D, window, scale, out, lse, reinterpret_cast<cudaStream_t>(stream),
+                     "tsk_mha_decode_paged", block_table, max_blocks_per_seq, page_size, num_pages);
 }

@@ -148,6 +148,37 @@ TSK_API tsk_status tsk_mha_decode_kvcache(const void *q, const void *k, const vo
                                          int32_t Hq, int32_t Hkv, int32_t D, int32_t window,
                                          float scale, void *out, float *lse, tsk_stream_t stream);
 
+/*
+ * Paged key/value cache.  The cache is a pool of fixed-size pages: k_pages and
+ * v_pages are bf16 [num_pages, page_size, Hkv, D]; block_table is an int32
+ * [num_seqs, max_blocks_per_seq] device array whose row s lists the pages of
+ * sequence s in order (key position x of the sequence is slot x % page_size
+ * of page block_table[s][x / page_size]).  page_size is 8, 16, 32, 64 or a
+ * multiple of 128 (a 128-key tile is then loaded as whole pages or one page
+ * part).  cu_seqlens_k holds the prefix sums of the key counts (not pool
+ * offsets); every page a sequence needs must be in [0, num_pages) and
+ * ceil(Lk / page_size) <= max_blocks_per_seq, else TSK_ERR_BAD_SEQLENS (via
+ * tsk_get_device_status) and nothing is computed.  Slots past Lk in a
+ * sequence's last page are read (with zero weight) and must hold finite
+ * values, e.g. a zero-initialised pool.  Other arguments and results as in
+ * tsk_mha_prefill_kvcache / tsk_mha_decode_kvcache.
+ */
+TSK_API tsk_status tsk_mha_prefill_paged(const void *q, const void *k_pages, const void *v_pages,
+                                        const float *sinks, const int32_t *cu_seqlens_q,
+                                        const int32_t *cu_seqlens_k, const int32_t *block_table,
+                                        int32_t max_blocks_per_seq, int32_t page_size,
+                                        int32_t num_pages, int32_t num_seqs, int64_t total_q,
+                                        int64_t total_k, int32_t Hq, int32_t Hkv, int32_t D,
+                                        int32_t window, float scale, void *out, float *lse,
+                                        tsk_stream_t stream);
+TSK_API tsk_status tsk_mha_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                       const float *sinks, const int32_t *cu_seqlens_k,
+                                       const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       int32_t page_size, int32_t num_pages, int32_t num_seqs,
+                                       int64_t total_k, int32_t max_seqlen_k, int32_t Hq,
+                                       int32_t Hkv, int32_t D, int32_t window, float scale,
+                                       void *out, float *lse, tsk_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 TSK_API const char *tsk_status_string(tsk_status s);
 
