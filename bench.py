@@ -63,27 +63,28 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash(D=64):
-    """Hash of the device sources the attention kernel for head dimension D is
-    built from (the host file and the other head dimension's kernel excluded)."""
+def kernel_source_hash(D=64, decode=False):
+    """Hash of the device sources the timed kernel is built from (the host file
+    and the other kernels' own headers excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_attention_prefill_gb300", "csrc")
-    files = ["ptx.cuh", "schedule.cuh", "attention.cuh"] + (["attention_d128.cuh"] if D == 128 else [])
+    files = ["ptx.cuh", "schedule.cuh", "attention.cuh"]
+    files += ["decode.cuh"] if decode else (["attention_d128.cuh"] if D == 128 else [])
     for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, D=64):
-    """Per-launch DRAM bytes of the attention kernel from a committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
+def ncu_traffic(workload, D=64, decode=False):
+    """Per-launch DRAM bytes of the timed kernel from a committed ncu summary,
+    if it was taken on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
         e = d.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash(D):
+        if e and e.get("kernel_source_hash") == kernel_source_hash(D, decode):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -386,7 +387,7 @@ def main():
         # A stream over the cache (about 4 FLOP per byte): the HBM roof applies.
         achieved = w.algorithmic_bytes() / (attn_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name, D),
+                    "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name, D, True),
                     "peak_source": f"{peak_src} HBM copy bandwidth",
                     "algorithmic_bytes": w.algorithmic_bytes(),
                     "kernel": f"decode_split_kernel<{D}> + decode_merge_kernel<{D}>"}
@@ -425,7 +426,7 @@ def main():
                 "matches_resident_run": bool(same)},
         "gpu_launches": args.steps * (3 if decode else pkg.tsk_kernels_per_call()),
         "clocks": clk.summary(),
-        "kernel_source_hash": kernel_source_hash(D),
+        "kernel_source_hash": kernel_source_hash(D, decode),
     }
     if not args.no_cpu_baseline:
         r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds)
