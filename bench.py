@@ -63,19 +63,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash(D=64, decode=False):
+def kernel_source_hash(D=64, decode=False, fp8=False):
     """Hash of the device sources the timed kernel is built from (the host file
     and the other kernels' own headers excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_attention_prefill_gb300", "csrc")
     files = ["ptx.cuh", "schedule.cuh", "attention.cuh"]
-    files += ["decode.cuh"] if decode else (["attention_d128.cuh"] if D == 128 else [])
+    files += (["decode.cuh"] if decode else ["attention_fp8.cuh"] if fp8 else
+              ["attention_d128.cuh"] if D == 128 else [])
     for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, D=64, decode=False):
+def ncu_traffic(workload, D=64, decode=False, fp8=False):
     """Per-launch DRAM bytes of the timed kernel from a committed ncu summary,
     if it was taken on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -84,7 +85,7 @@ def ncu_traffic(workload, D=64, decode=False):
     try:
         d = json.load(open(p))
         e = d.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash(D, decode):
+        if e and e.get("kernel_source_hash") == kernel_source_hash(D, decode, fp8):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -274,9 +275,13 @@ def main():
     flops = w.unmasked_flops()
 
     # host (pinned) and device copies
-    h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_k = torch.from_numpy(w.k.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_v = torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    fp8 = w.fp8 is not None  # E4M3 inputs with per-tensor scales
+    if fp8:
+        h_q, h_k, h_v = (torch.from_numpy(w.fp8[n]).pin_memory() for n in ("q", "k", "v"))
+    else:
+        h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_k = torch.from_numpy(w.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_v = torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).pin_memory()
     h_s = torch.from_numpy(w.sinks).pin_memory()
     h_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
     kvcache = w.cu_seqlens_k is not None
@@ -284,12 +289,17 @@ def main():
     h_cuk = torch.from_numpy(w.cu_seqlens_k if kvcache else w.cu_seqlens).pin_memory()
     q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
     sinks, cu, cuk = h_s.to(dev), h_cu.to(dev), h_cuk.to(dev)
-    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)  # bf16 for every input type
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def step(o=out, l=lse, qq=q, kk=k, vv=v, ss=sinks, cc=cu, ck=cuk):
-        if decode:
+        if fp8:
+            f = w.fp8
+            rc = pkg.tsk_mha_prefill_fp8(qq, kk, vv, f["q_scale"], f["k_scale"], f["v_scale"], ss,
+                                         cc, w.num_seqs, T, Hq, Hkv, D, w.window, w.scale, o, l,
+                                         stream)
+        elif decode:
             rc = pkg.tsk_mha_decode_kvcache(qq, kk, vv, ss, ck, w.num_seqs, w.total_keys,
                                             max(w.seqlens_k), Hq, Hkv, D, w.window, w.scale, o, l,
                                             stream)
@@ -393,18 +403,23 @@ def main():
                     "kernel": f"decode_split_kernel<{D}> + decode_merge_kernel<{D}>"}
     else:
         achieved = flops / (attn_avg * 1e-3) / 1e12
+        # E4M3 contractions: twice the dense bf16 rate (the nominal fp8/bf16 ratio)
+        peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
         roofline = {"bound": "tensor", "achieved": achieved,
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(w.name, D),
-                    "peak_source": f"{peak_src} dense bf16 (burst)",
+                    "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": ncu_traffic(w.name, D, False, fp8),
+                    "peak_source": (f"{peak_src} dense bf16 (burst) x 2 for E4M3" if fp8 else
+                                    f"{peak_src} dense bf16 (burst)"),
                     "algorithmic_bytes": w.algorithmic_bytes(),
-                    "kernel": ("attention_fwd_d128_kernel" if D == 128 else
+                    "kernel": ("attention_fwd_fp8_kernel" if fp8 else
+                               "attention_fwd_d128_kernel" if D == 128 else
                                "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
                                "attention_fwd_kernel<false>")}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (fp32 accumulation)" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, fp32 sinks)",
         "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
                    f"{len(w.seqlens)} seqs", "total_tokens": T,
@@ -426,7 +441,7 @@ def main():
                 "matches_resident_run": bool(same)},
         "gpu_launches": args.steps * (3 if decode else pkg.tsk_kernels_per_call()),
         "clocks": clk.summary(),
-        "kernel_source_hash": kernel_source_hash(D, decode),
+        "kernel_source_hash": kernel_source_hash(D, decode, fp8),
     }
     if not args.no_cpu_baseline:
         r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds)

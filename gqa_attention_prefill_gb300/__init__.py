@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "tsk_mha_prefill_kvcache",
-           "tsk_mha_decode_kvcache", "tsk_mha_prefill_paged", "tsk_mha_decode_paged", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
+           "tsk_mha_decode_kvcache", "tsk_mha_prefill_paged", "tsk_mha_decode_paged", "tsk_mha_prefill_fp8", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
            "tsk_get_device_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
@@ -87,6 +87,10 @@ def load_library():
         lib.tsk_mha_decode_paged.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i32, i32,
                                              i32, i32, i32, ctypes.c_float, P, P, P]
         lib.tsk_mha_decode_paged.restype = ctypes.c_int
+        f32 = ctypes.c_float
+        lib.tsk_mha_prefill_fp8.argtypes = [P, P, P, f32, f32, f32, P, P, i32, i64, i32, i32, i32,
+                                            i32, f32, P, P, P]
+        lib.tsk_mha_prefill_fp8.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
         lib.tsk_last_error.argtypes = []
@@ -210,6 +214,17 @@ def tsk_mha_decode_paged(q, k_pages, v_pages, sinks, cu_seqlens_k, block_table, 
                                     int(page_size), int(num_pages), int(num_seqs), int(total_k),
                                     int(max_seqlen_k), int(Hq), int(Hkv), int(D), int(window),
                                     float(scale), _ptr(out), _ptr(lse), _stream_handle(stream))
+
+
+def tsk_mha_prefill_fp8(q8, k8, v8, q_scale, k_scale, v_scale, sinks, cu_seqlens, num_seqs,
+                        total_tokens, Hq, Hkv, D, window, scale, out, lse, stream=None) -> int:
+    """Prefill with E4M3 inputs and per-tensor scales (same arguments as the C
+    function; q8/k8/v8 are uint8 tensors or addresses).  Returns the status."""
+    lib = load_library()
+    return lib.tsk_mha_prefill_fp8(_ptr(q8), _ptr(k8), _ptr(v8), float(q_scale), float(k_scale),
+                                   float(v_scale), _ptr(sinks), _ptr(cu_seqlens), int(num_seqs),
+                                   int(total_tokens), int(Hq), int(Hkv), int(D), int(window),
+                                   float(scale), _ptr(out), _ptr(lse), _stream_handle(stream))
 
 
 def mha_decode_kvcache(q, k, v, cu_seqlens_k, max_seqlen_k: int, sinks=None, window: int = 0,

@@ -17,6 +17,7 @@
 #include "attention.cuh"
 #include "attention_d128.cuh"
 #include "decode.cuh"
+#include "attention_fp8.cuh"
 #include "schedule.cuh"
 
 namespace {
@@ -30,6 +31,8 @@ struct Workspace {
   int max_seqs = 0;
   float* part = nullptr;  // decode: per-split partial states
   size_t part_bytes = 0;
+  uint8_t* vt = nullptr;  // FP8 prefill: transposed V
+  size_t vt_bytes = 0;
 };
 
 struct DeviceState {
@@ -92,6 +95,20 @@ tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int D,
   return r == CUDA_SUCCESS ? TSK_OK : TSK_ERR_DEVICE;
 }
 
+// A 3-D uint8 tensor (innermost first) with a box of box0 x box1 x 1 and the
+// given swizzle.
+tsk_status encode_u8(CUtensorMap* m, const void* ptr, const cuuint64_t dims[3],
+                     const cuuint64_t strides[2], cuuint32_t box0, cuuint32_t box1,
+                     CUtensorMapSwizzle swz) {
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr),
+                        const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides), box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TSK_OK : TSK_ERR_DEVICE;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -123,6 +140,10 @@ tsk_status check_device(int* dev_out, DeviceState** st_out) {
       e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::d128::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::fp8::attention_fwd_fp8_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::fp8::kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tsk::dec::decode_split_kernel<64>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -467,6 +488,7 @@ tsk_status tsk_release(void) {
     if (kv.second.base || kv.second.part) cudaSetDevice(kv.first.first);
     if (kv.second.base) cudaFree(kv.second.base);
     if (kv.second.part) cudaFree(kv.second.part);
+    if (kv.second.vt) cudaFree(kv.second.vt);
   }
   if (dev >= 0) cudaSetDevice(dev);
   g_ws.clear();
@@ -779,4 +801,144 @@ extern "C" tsk_status tsk_mha_decode_paged(const void* q, const void* k_pages, c
   return decode_impl(q, k_pages, v_pages, sinks, cu_seqlens_k, num_seqs, total_k, max_seqlen_k,
                      Hq, Hkv, D, window, scale, out, lse, reinterpret_cast<cudaStream_t>(stream),
                      "tsk_mha_decode_paged", block_table, max_blocks_per_seq, page_size, num_pages);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) prefill, head dimension 64.
+extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const void* v8,
+                                          float q_scale, float k_scale, float v_scale,
+                                          const float* sinks, const int32_t* cu_seqlens,
+                                          int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                          int32_t Hkv, int32_t D, int32_t window, float scale,
+                                          void* out, float* lse, tsk_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!q8 || !k8 || !v8 || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+  for (float x : {scale, q_scale, k_scale, v_scale})
+    if (!std::isfinite(x) || !(x > 0.f)) return TSK_ERR_INVALID_ARG;
+  if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
+    return TSK_ERR_UNSUPPORTED;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
+  if (!a16(q8) || !a16(k8) || !a16(v8) || !a16(out)) return TSK_ERR_ALIGNMENT;
+  if (!a4(cu_seqlens) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
+  const size_t out_bytes = (size_t)total_tokens * Hq * D * 2;
+  const size_t q_bytes = (size_t)total_tokens * Hq * D, kv_bytes = (size_t)total_tokens * Hkv * D;
+  if (total_tokens > 0 && (overlaps(out, out_bytes, q8, q_bytes) ||
+                           overlaps(out, out_bytes, k8, kv_bytes) ||
+                           overlaps(out, out_bytes, v8, kv_bytes)))
+    return TSK_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  DeviceState* ds = nullptr;
+  tsk_status st = check_device(&dev, &ds);
+  if (st != TSK_OK) return st;
+  if ((st = get_encoder()) != TSK_OK) return st;
+  const int64_t max_tiles64 = total_tokens / tsk::kTileM + num_seqs + 1;
+  const int max_tiles = (int)max_tiles64;
+  Workspace* ws = nullptr;
+  if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
+  // Transposed V: [Hkv][64][t_pad] bytes, t_pad = 128 x (query-tile bound).
+  const int64_t t_pad = (int64_t)ws->max_tiles * 128;
+  const size_t vt_need = (size_t)Hkv * 64 * (size_t)t_pad;
+  if (ws->vt_bytes < vt_need) {
+    uint8_t* nb = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), vt_need, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "FP8 V^T buffer");
+    if (ws->vt) cudaFreeAsync(ws->vt, stream);
+    ws->vt = nb;
+    ws->vt_bytes = vt_need;
+  }
+
+  CUtensorMap tq, tk, tvt, to;
+  {
+    const cuuint64_t dq[3] = {64, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
+    const cuuint64_t sq[2] = {64, (cuuint64_t)Hq * 64};
+    const cuuint64_t dk[3] = {64, (cuuint64_t)Hkv, (cuuint64_t)total_tokens};
+    const cuuint64_t sk[2] = {64, (cuuint64_t)Hkv * 64};
+    // Q/K boxes: 64 bytes x 1 head x 128 rows (the second box dimension is the head)
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q8),
+                          const_cast<cuuint64_t*>(dq), const_cast<cuuint64_t*>(sq), box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+      r = g_encode(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(k8),
+                   const_cast<cuuint64_t*>(dk), const_cast<cuuint64_t*>(sk), box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return TSK_ERR_DEVICE;
+    const cuuint64_t dv[3] = {(cuuint64_t)t_pad, 64, (cuuint64_t)Hkv};
+    const cuuint64_t sv[2] = {(cuuint64_t)t_pad, (cuuint64_t)t_pad * 64};
+    if ((st = encode_u8(&tvt, ws->vt, dv, sv, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != TSK_OK)
+      return st;
+    if ((st = encode_thd(&to, out, total_tokens, Hq, 64, 32)) != TSK_OK) return st;
+  }
+
+  char name[112];
+  snprintf(name, sizeof name, "tsk_mha_prefill_fp8[Hq=%d,Hkv=%d,W=%d,nseq=%d,T=%lld]", Hq, Hkv,
+           window, num_seqs, (long long)total_tokens);
+  nvtxRangePushA(name);
+  const size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ws->max_seqs + 1 + 3) & ~(size_t)3;
+  int* tile_off = ws->base + tsk::kWsHeader;
+  int4* list = reinterpret_cast<int4*>(ws->base + off_ints);
+  const bool prof = g_profile;
+  if (prof) {
+    if (g_ev_dev != dev) {
+      for (auto& e : g_ev) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
+      }
+      for (auto& e : g_ev)
+        if (cudaEventCreate(&e) != cudaSuccess) {
+          nvtxRangePop();
+          return TSK_ERR_DEVICE;
+        }
+      g_ev_dev = dev;
+    }
+    cudaEventRecord(g_ev[0], stream);
+  }
+  tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
+      cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, ws->base,
+      tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0});
+  tsk::fp8::fp8_vt_kernel<<<dim3(max_tiles, Hkv), 128, 0, stream>>>(
+      reinterpret_cast<const uint8_t*>(v8), cu_seqlens, tile_off, ws->base, num_seqs, Hkv, ws->vt,
+      t_pad);
+  if (prof) cudaEventRecord(g_ev[1], stream);
+
+  tsk::fp8::Fp8Params f;
+  tsk::AttnParams& p = f.a;
+  p.sinks = sinks;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.list = list;
+  p.ws = ws->base;
+  p.status = ws->base + tsk::kWsStatus;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.HP = (p.G + 1) / 2;
+  p.window = window;
+  p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.debug_stall = g_debug_stall;
+  p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
+  f.tile_off = tile_off;
+  f.v_scale = v_scale;
+  const int64_t units_bound = max_tiles64 * Hkv * p.HP;
+  const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
+  tsk::fp8::attention_fwd_fp8_kernel<<<grid, tsk::kThreads, tsk::fp8::kSmemBytes, stream>>>(
+      tq, tk, tvt, to, f);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) note_error("FP8 attention kernel launch", e);
+  if (prof) {
+    cudaEventRecord(g_ev[2], stream);
+    g_ev_recorded = true;
+  }
+  nvtxRangePop();
+  return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
 }

@@ -179,6 +179,27 @@ TSK_API tsk_status tsk_mha_decode_paged(const void *q, const void *k_pages, cons
                                        int32_t Hkv, int32_t D, int32_t window, float scale,
                                        void *out, float *lse, tsk_stream_t stream);
 
+/*
+ * tsk_mha_prefill_fp8 -- tsk_mha_prefill with FP8 inputs (the pages' model
+ * serves FP8 weights; no formula is given for attention inputs): q8, k8, v8
+ * are OCP E4M3 codes ([total_tokens, Hq, 64] and [total_tokens, Hkv, 64]
+ * bytes) whose values are code * q_scale, code * k_scale, code * v_scale
+ * (per-tensor fp32 scales, finite and > 0).  The result is the attention of
+ * those values (scale, sinks, window, lse and out as in tsk_mha_prefill; out
+ * stays bf16).  Head dimension 64 only.  P is rounded to E4M3 for the PV
+ * product (error up to p / 16, or 2^-10 for p < 2^-6), so outputs differ
+ * from the exact attention of the dequantised inputs by up to
+ * sum_j max(p_j / 16, 2^-10) |v_j| / l per element plus bf16 rounding; lse
+ * is not affected.  Extra device memory per (device, stream): a transposed copy of
+ * V padded to 128-key tiles.
+ */
+TSK_API tsk_status tsk_mha_prefill_fp8(const void *q8, const void *k8, const void *v8,
+                                      float q_scale, float k_scale, float v_scale,
+                                      const float *sinks, const int32_t *cu_seqlens,
+                                      int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                      int32_t Hkv, int32_t D, int32_t window, float scale,
+                                      void *out, float *lse, tsk_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 TSK_API const char *tsk_status_string(tsk_status s);
 

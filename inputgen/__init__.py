@@ -118,6 +118,9 @@ class Workload:
     # new tokens' keys last; None for plain prefill (keys == queries)
     cu_seqlens_k: np.ndarray | None = None
     seqlens_k: list | None = None
+    # FP8 inputs (E4M3 codes, per-tensor power-of-two scales): q/k/v above are
+    # then the exact bf16 values code * scale; None for bf16 inputs
+    fp8: dict | None = None
 
     @property
     def total_tokens(self) -> int:
@@ -151,6 +154,76 @@ class Workload:
         """Read Q, K, V once; write out (bf16) and lse (fp32) once."""
         T, Tk = self.total_tokens, self.total_keys
         return T * (2 * self.Hq * self.D * 2 + 4 * self.Hq) + Tk * 2 * self.Hkv * self.D * 2
+
+
+# --------------------------------------------------------------------- FP8
+# OCP FP8 E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits; largest
+# finite 448, no infinities, all-ones = NaN; subnormals down to 2^-9.
+E4M3_MAX = 448.0
+
+
+def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """uint8 E4M3 codes of float32 `x`, round to nearest even, saturating to
+    +-448 (NaN -> 0x7F)."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = (np.signbit(x)).astype(np.uint8) << 7
+    a = np.minimum(np.abs(np.nan_to_num(x, nan=0.0)), E4M3_MAX)
+    # exponent of the binade, clamped to the normal range [-6, 8]; below 2^-6
+    # the spacing stays 2^-9 (subnormals)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)
+    quantum = np.exp2(e - 3)
+    m = np.round(a / quantum)            # numpy rounds halves to even
+    q = m * quantum                      # the representable value
+    q = np.minimum(q, E4M3_MAX)
+    # re-derive the fields from q (a carry may have moved it to the next binade)
+    eq = np.floor(np.log2(np.where(q > 0, q, 1.0)))
+    normal = q >= 2.0 ** -6
+    exp_field = np.where(normal, eq + 7, 0).astype(np.int64)
+    man_field = np.where(normal, q / np.exp2(eq) * 8 - 8, q / 2.0 ** -9).astype(np.int64)
+    code = (exp_field << 3 | man_field).astype(np.uint8) | sign
+    code[np.isnan(x)] = 0x7F
+    return code
+
+
+def e4m3_to_f32(code: np.ndarray) -> np.ndarray:
+    """float32 values of uint8 E4M3 codes."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    v = np.where((c & 0x7F) == 0x7F, np.nan, v)
+    return (s * v).astype(np.float32)
+
+
+def quantize_e4m3(x: np.ndarray):
+    """(codes, scale): a power-of-two scale with max|x| / scale <= 448 and the
+    E4M3 codes of x / scale."""
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    scale = 2.0 ** np.ceil(np.log2(amax / E4M3_MAX)) if amax > 0 else 1.0
+    return f32_to_e4m3(x.astype(np.float64) / scale), float(scale)
+
+
+def make_fp8(seqlens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, sink_sigma=1.0,
+             k_mult=1.0, with_sinks=True, name="fp8") -> Workload:
+    """As `make`, with Q, K, V drawn in fp32 and quantized to E4M3 with
+    per-tensor power-of-two scales; w.q/k/v hold the exact dequantized values
+    (as bf16, which represents every E4M3 value times a power of two)."""
+    seqlens = [int(x) for x in seqlens]
+    cu = np.zeros(len(seqlens) + 1, dtype=np.int32)
+    if seqlens:
+        cu[1:] = np.cumsum(np.asarray(seqlens, dtype=np.int64)).astype(np.int32)
+    T = int(cu[-1])
+    qf = normal_f32(seed, STREAM_Q, (T, Hq, D))
+    kf = normal_f32(seed, STREAM_K, (T, Hkv, D), k_mult)
+    vf = normal_f32(seed, STREAM_V, (T, Hkv, D))
+    (q8, sq), (k8, sk), (v8, sv) = quantize_e4m3(qf), quantize_e4m3(kf), quantize_e4m3(vf)
+    deq = lambda c, sc: f32_to_bf16_bits(e4m3_to_f32(c) * np.float32(sc))
+    sinks = normal_f32(seed, STREAM_SINKS, (Hq,), sink_sigma) if with_sinks else None
+    return Workload(name, seqlens, Hq, Hkv, D, window, scale, deq(q8, sq), deq(k8, sk),
+                    deq(v8, sv), sinks, cu, seed,
+                    fp8=dict(q=q8, k=k8, v=v8, q_scale=sq, k_scale=sk, v_scale=sv))
 
 
 def make(seqlens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, sink_sigma=1.0,
@@ -208,6 +281,9 @@ CONFIGS = {
                                        "Hkv=8, D=64, sinks N(0,1), causal"),
     "decode_ragged32_h64kv8": dict(desc="32 seqs, one query token each over U{512..32768} keys, "
                                         "Hq=64, Hkv=8, D=64, sinks N(0,2), causal"),
+    # FP8 (E4M3) Q/K/V with per-tensor scales, otherwise the bench workload
+    "fp8_causal_4x4096_h64kv8": dict(desc="as causal_4x4096 with E4M3 Q/K/V (per-tensor "
+                                          "power-of-two scales)"),
     # head dimension 128 (the same unmasked FLOPs as causal_4x4096_h64kv8)
     "causal_4x4096_h32kv8_d128": dict(desc="4 seqs x 4096 tokens, Hq=32, Hkv=8, D=128, "
                                            "sinks N(0,1), scale 1/sqrt(128), full causal"),
@@ -240,6 +316,8 @@ def config(name: str, seed: int = 0) -> Workload:
     if name == "decode_ragged32_h64kv8":
         return make_kvcache([1] * 32, ragged_lengths(seed, 32, 512, 32768), 64, 8, sink_sigma=2.0,
                             seed=seed, name=name)
+    if name == "fp8_causal_4x4096_h64kv8":
+        return make_fp8([4096] * 4, 64, 8, seed=seed, name=name)
     if name == "causal_4x4096_h32kv8_d128":
         return make([4096] * 4, 32, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
     if name == "long_1x32768_h32kv8_d128":

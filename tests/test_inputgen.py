@@ -1,5 +1,6 @@
 """Seeded input generator (no GPU)."""
 import numpy as np
+import pytest
 
 import inputgen
 
@@ -71,3 +72,34 @@ def test_sample_rows_cover_structure():
     assert {127, 128, 255, 256}.issubset(toks)
     assert set(h.tolist()) == set(range(8))
     assert len(rows) == len(t) >= 200
+
+
+def test_e4m3_decode_matches_torch():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    mine = inputgen.e4m3_to_f32(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(mine)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_rne():
+    torch = pytest.importorskip("torch")
+    vals = inputgen.e4m3_to_f32(np.arange(256, dtype=np.uint8))
+    vals = np.unique(vals[~np.isnan(vals)])
+    mids = (vals[:-1] + vals[1:]) / 2          # ties: round to even
+    x = np.concatenate([inputgen.normal_f32(3, 77, (100000,), 40.0), vals, mids]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(inputgen.f32_to_e4m3(x), ref)
+    assert inputgen.f32_to_e4m3(np.array([1e6, -1e6], np.float32)).tolist() == [0x7E, 0xFE]
+
+
+def test_fp8_workload_dequantizes_exactly_in_bf16():
+    w = inputgen.make_fp8([100, 37], 4, 2, seed=5)
+    for name in ("q", "k", "v"):
+        exact = inputgen.e4m3_to_f32(w.fp8[name]) * np.float32(w.fp8[name + "_scale"])
+        assert np.array_equal(inputgen.bf16_bits_to_f32(getattr(w, name)), exact)
+        assert np.log2(w.fp8[name + "_scale"]) == np.round(np.log2(w.fp8[name + "_scale"]))
