@@ -151,9 +151,12 @@ class Workload:
         return 4.0 * self.D * self.Hq * self.allowed_keys()
 
     def algorithmic_bytes(self) -> int:
-        """Read Q, K, V once; write out (bf16) and lse (fp32) once."""
+        """Read Q, K, V once (2 bytes per element, 1 for FP8 inputs); write out
+        (bf16) and lse (fp32) once."""
         T, Tk = self.total_tokens, self.total_keys
-        return T * (2 * self.Hq * self.D * 2 + 4 * self.Hq) + Tk * 2 * self.Hkv * self.D * 2
+        b = 1 if self.fp8 is not None else 2
+        return (T * (self.Hq * self.D * (b + 2) + 4 * self.Hq) +
+                Tk * 2 * self.Hkv * self.D * b)
 
 
 # --------------------------------------------------------------------- FP8
