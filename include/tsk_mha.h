@@ -80,6 +80,12 @@ typedef enum {
  * (device, stream), created on first use; calls on one stream are ordered,
  * calls on different streams do not share it.  Not safe to call concurrently
  * from several host threads on the same stream.
+ * CUDA graphs: once a stream's workspace is warm (an earlier eager call on
+ * that stream with at least as many query tiles and sequences), a call
+ * enqueues kernel launches only and may be captured on that stream.  The
+ * graph keeps using that stream's workspace, so its replays must not overlap
+ * other calls on the same stream; a replay reads the inputs the buffers hold
+ * when it runs.  The same holds for every entry point below.
  */
 TSK_API tsk_status tsk_mha_prefill(const void *q, const void *k, const void *v, const float *sinks,
                            const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
