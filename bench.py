@@ -6,9 +6,11 @@ number through the C ABI with host buffers, and the CPU oracle as a baseline.
   python bench.py --impl reference ...    # the CPU oracle as the reference arm
 
 One step = one tsk_mha_prefill call (scheduler pre-pass + attention kernel)
-over the whole workload, inputs resident in HBM.  L2 is flushed (a 256 MB
-write) before every timed step; only the step itself is inside the CUDA
-events.  Under torchrun (N > 1) every rank runs an independent replica on its
+over the whole workload, inputs resident in HBM.  L2 is flushed before every
+timed step: a 256 MB write, then a 256 MB read of another buffer, so that
+the written lines are evicted (written back to HBM) before the step starts
+and the step finds a cold L2 without paying for the flush's write-backs;
+only the step itself is inside the CUDA events.  Under torchrun (N > 1) every rank runs an independent replica on its
 own GPU (the operation has no cross-GPU exchange); value = all ranks' FLOPs /
 the slowest rank's time.
 """
@@ -292,6 +294,11 @@ def main():
     out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)  # bf16 for every input type
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    evict = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()   # 256 MB of dirty lines replace the L2's contents
+        evict.sum()     # a 256 MB read writes them back before the next step
 
     def step(o=out, l=lse, qq=q, kk=k, vv=v, ss=sinks, cc=cu, ck=cuk):
         if fp8:
@@ -314,7 +321,7 @@ def main():
 
     pkg.tsk_profile_enable(True)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     st = pkg.tsk_get_device_status(stream)
@@ -330,7 +337,7 @@ def main():
     with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                       else local) as clk:
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -371,7 +378,7 @@ def main():
     torch.cuda.synchronize()
     e_ms = []
     for _ in range(args.e2e_steps):
-        flush.zero_()
+        flush_l2()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         e2e_step()
@@ -428,7 +435,7 @@ def main():
                                     else None)),
                    "Hq": Hq, "Hkv": Hkv, "D": D,
                    "window": w.window, "scale": w.scale, "sinks": True, "lse": True,
-                   "l2": "flushed before every timed step (256 MB write)",
+                   "l2": "flushed before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "tokens_per_s": T * ws / (ms * 1e-3),
         "pct_of_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
