@@ -75,6 +75,8 @@ def load_library():
         lib.tsk_mha_prefill.restype = ctypes.c_int
         lib.tsk_mha_prefill_noalloc.argtypes = lib.tsk_mha_prefill.argtypes
         lib.tsk_mha_prefill_noalloc.restype = ctypes.c_int
+        lib.tsk_mha_prefill_host.argtypes = lib.tsk_mha_prefill.argtypes
+        lib.tsk_mha_prefill_host.restype = ctypes.c_int
         lib.tsk_mha_prefill_kvcache.argtypes = [P, P, P, P, P, P, i32, i64, i64, i32, i32, i32,
                                                 i32, ctypes.c_float, P, P, P]
         lib.tsk_mha_prefill_kvcache.restype = ctypes.c_int
@@ -119,7 +121,9 @@ def _ptr(x):
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data  # numpy array (host memory)
 
 
 def _stream_handle(stream):
@@ -148,6 +152,20 @@ def tsk_mha_prefill(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, Hq, Hkv,
                                int(num_seqs), int(total_tokens), int(Hq), int(Hkv), int(D),
                                int(window), float(scale), _ptr(out), _ptr(lse),
                                _stream_handle(stream))
+
+
+def tsk_mha_prefill_host(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, Hq, Hkv, D, window,
+                         scale, out, lse, stream=None) -> int:
+    """``tsk_mha_prefill`` with every buffer in host memory (CPU tensors,
+    numpy arrays or raw host addresses; page-locked for overlapped copies).
+    The library pipelines chunked copies in, attention and copies out; the
+    call is asynchronous: read ``out``/``lse`` after ``stream`` (default: the
+    current stream) has been synchronised.  Returns the status code."""
+    lib = load_library()
+    return lib.tsk_mha_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens),
+                                    int(num_seqs), int(total_tokens), int(Hq), int(Hkv), int(D),
+                                    int(window), float(scale), _ptr(out), _ptr(lse),
+                                    _stream_handle(stream))
 
 
 def tsk_mha_prefill_noalloc(q, k, v, sinks, cu_seqlens, num_seqs, total_tokens, Hq, Hkv, D,

@@ -12,6 +12,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "tsk_mha.h"
 #include "attention.cuh"
@@ -44,6 +45,17 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// Host-buffer pipeline (tsk_mha_prefill_host), one per (device, caller
+// stream): its own copy and compute streams and a grow-only device buffer
+// that holds the call's inputs and outputs.
+struct HostPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp[2] = {nullptr, nullptr};
+  uint8_t* buf = nullptr;
+  size_t cap = 0;
+};
+std::mutex g_pipe_mu;  // held for a whole tsk_mha_prefill_host call (never inside g_mu)
+std::map<std::pair<int, cudaStream_t>, HostPipe> g_pipe;
 std::map<int, DeviceState> g_dev;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -481,9 +493,28 @@ tsk_status tsk_profile_read(float* prepass_ms, float* attention_ms) {
 }
 
 tsk_status tsk_release(void) {
+  std::lock_guard<std::mutex> plock(g_pipe_mu);
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = -1;
-  if (!g_ws.empty() && cudaGetDevice(&dev) == cudaSuccess) cudaDeviceSynchronize();
+  if ((!g_ws.empty() || !g_pipe.empty()) && cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceSynchronize();
+  for (auto& kv : g_pipe) {
+    HostPipe& hp = kv.second;
+    cudaSetDevice(kv.first.first);
+    cudaStreamSynchronize(kv.first.second);
+    if (hp.buf) cudaFree(hp.buf);
+    for (cudaStream_t st : {hp.h2d, hp.d2h, hp.comp[0], hp.comp[1]}) {
+      auto it = g_ws.find({kv.first.first, st});
+      if (it != g_ws.end()) {
+        if (it->second.base) cudaFree(it->second.base);
+        if (it->second.part) cudaFree(it->second.part);
+        if (it->second.vt) cudaFree(it->second.vt);
+        g_ws.erase(it);
+      }
+      if (st) cudaStreamDestroy(st);
+    }
+  }
+  g_pipe.clear();
   for (auto& kv : g_ws) {
     if (kv.second.base || kv.second.part) cudaSetDevice(kv.first.first);
     if (kv.second.base) cudaFree(kv.second.base);
@@ -941,4 +972,218 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   }
   nvtxRangePop();
   return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Host buffers in, host buffers out: tsk_mha_prefill_host.
+//
+// The packed token stream is cut into chunks of consecutive tokens.  Chunk c
+// covers tokens [t_c, t_{c+1}); for every sequence it touches, its queries
+// are the sequence's rows inside the chunk and its keys are the sequence's
+// rows from its start up to the chunk's end, which earlier chunks (and this
+// one) have already copied to the device.  So each chunk is one prefill over
+// a key/value cache (the same kernels as tsk_mha_prefill_kvcache), and the
+// three stages overlap across chunks: the copy of chunk c+1's inputs, the
+// attention of chunk c (two compute streams, so one chunk's tail overlaps the
+// next chunk's start) and the copy of chunk c-1's outputs.
+namespace {
+
+__global__ void merge_status_kernel(int* dst, int* a, int* b) {
+  int* const srcs[2] = {a, b};
+  for (int j = 0; j < 2; ++j) {
+    int* src = srcs[j];
+    if (src == nullptr || src[tsk::kWsStatus] == 0) continue;
+    if (dst[tsk::kWsStatus] == 0)
+      for (int i = 0; i < 3; ++i) dst[tsk::kWsStatus + i] = src[tsk::kWsStatus + i];
+    for (int i = 0; i < 3; ++i) src[tsk::kWsStatus + i] = 0;
+  }
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Chunk boundaries and, per chunk, the kvcache-call description.
+struct HostChunk {
+  int64_t t0, t1;      // token rows [t0, t1)
+  int64_t k0;          // first key row: start of the chunk's first sequence
+  int32_t nseq;        // sequences with at least one query row in the chunk
+  size_t cu_off;       // index of the chunk's cu_q (nseq + 1) then cu_k (nseq + 1)
+};
+
+}  // namespace
+
+extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const void* v,
+                                           const float* sinks, const int32_t* cu_seqlens,
+                                           int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                           int32_t Hkv, int32_t D, int32_t window, float scale,
+                                           void* out, float* lse, tsk_stream_t stream_) {
+  // ---- host-only checks (the offsets are host memory here, so all of them)
+  if (!q || !k || !v || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TSK_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
+    return TSK_ERR_UNSUPPORTED;
+  if (cu_seqlens[0] != 0 || (int64_t)cu_seqlens[num_seqs] != total_tokens)
+    return TSK_ERR_INVALID_ARG;
+  for (int32_t s = 0; s < num_seqs; ++s)
+    if (cu_seqlens[s + 1] < cu_seqlens[s]) return TSK_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  // ---- chunks: about eight of at least 2048 tokens.  A chunk ends at a
+  // sequence end or 128 rows after a query-tile start of the sequence it
+  // cuts, so that every query tile (and every warp's 32 rows) is the one
+  // tsk_mha_prefill forms: the results are then bit for bit the same.
+  const int64_t T = total_tokens;
+  int64_t chunk = (T + 7) / 8;
+  if (chunk < 2048) chunk = 2048;
+  std::vector<HostChunk> chunks;
+  std::vector<int32_t> cu_host;
+  {
+    int32_t s = 0, s1 = 0;
+    for (int64_t t0 = 0, t1 = 0; t0 < T; t0 = t1) {
+      t1 = t0 + chunk < T ? t0 + chunk : T;
+      if (t1 < T) {
+        while (cu_seqlens[s1 + 1] <= t1) ++s1;  // the sequence holding row t1
+        const int64_t off = t1 - cu_seqlens[s1];
+        if (off % tsk::kTileM != 0) {
+          const int64_t up = cu_seqlens[s1] + (off / tsk::kTileM + 1) * tsk::kTileM;
+          t1 = up < cu_seqlens[s1 + 1] ? up : cu_seqlens[s1 + 1];
+        }
+      }
+      while (cu_seqlens[s + 1] <= t0) ++s;  // the sequence holding row t0
+      HostChunk c{t0, t1, cu_seqlens[s], 0, cu_host.size()};
+      std::vector<int32_t> cq{0}, ck{0};
+      for (int32_t r = s; r < num_seqs && cu_seqlens[r] < t1; ++r) {
+        const int64_t a = cu_seqlens[r] > t0 ? cu_seqlens[r] : t0;
+        const int64_t b = cu_seqlens[r + 1] < t1 ? cu_seqlens[r + 1] : t1;
+        if (b <= a) continue;  // empty sequence
+        cq.push_back((int32_t)(b - t0));
+        ck.push_back((int32_t)(b - c.k0));
+      }
+      c.nseq = (int32_t)cq.size() - 1;
+      cu_host.insert(cu_host.end(), cq.begin(), cq.end());
+      cu_host.insert(cu_host.end(), ck.begin(), ck.end());
+      chunks.push_back(c);
+    }
+  }
+
+  std::lock_guard<std::mutex> plock(g_pipe_mu);
+  int dev = -1;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    tsk_status st = check_device(&dev, &ds);
+    if (st != TSK_OK) return st;
+  }
+  HostPipe& hp = g_pipe[{dev, stream}];
+  if (!hp.h2d) {
+    for (cudaStream_t* st : {&hp.h2d, &hp.d2h, &hp.comp[0], &hp.comp[1]})
+      if (cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown, "host pipeline streams");
+  }
+
+  // ---- device buffer: q, k, v, out, lse, sinks, chunk offsets
+  const size_t q_bytes = (size_t)T * Hq * D * 2, kv_bytes = (size_t)T * Hkv * D * 2;
+  const size_t lse_bytes = lse ? (size_t)T * Hq * 4 : 0, sink_bytes = sinks ? (size_t)Hq * 4 : 0;
+  const size_t off_q = 0, off_k = align256(q_bytes), off_v = off_k + align256(kv_bytes),
+               off_o = off_v + align256(kv_bytes), off_l = off_o + align256(q_bytes),
+               off_s = off_l + align256(lse_bytes), off_c = off_s + align256(sink_bytes),
+               need = off_c + align256(cu_host.size() * 4);
+  if (hp.cap < need) {
+    if (hp.buf) {
+      cudaStreamSynchronize(stream);  // earlier calls on this stream may still use it
+      cudaFree(hp.buf);
+      hp.buf = nullptr;
+      hp.cap = 0;
+    }
+    if (cudaMalloc(reinterpret_cast<void**>(&hp.buf), need) != cudaSuccess)
+      return cuda_fail(cudaErrorMemoryAllocation, "host pipeline buffer");
+    hp.cap = need;
+  }
+  uint8_t* b = hp.buf;
+  const size_t qrow = (size_t)Hq * D * 2, kvrow = (size_t)Hkv * D * 2;
+
+  std::vector<cudaEvent_t> evs;
+  auto event = [&]() {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return e;
+    evs.push_back(e);
+    return e;
+  };
+  tsk_status st = TSK_OK;
+  cudaEvent_t ev_start = event(), ev_done = event();
+  if (!ev_start || !ev_done) st = cuda_fail(cudaErrorUnknown, "host pipeline events");
+  if (st == TSK_OK) {
+    // Everything starts after the work already queued on the caller's stream
+    // (earlier calls may still be reading the buffer).
+    cudaEventRecord(ev_start, stream);
+    for (cudaStream_t s2 : {hp.h2d, hp.d2h, hp.comp[0], hp.comp[1]})
+      cudaStreamWaitEvent(s2, ev_start, 0);
+    if (sinks) cudaMemcpyAsync(b + off_s, sinks, sink_bytes, cudaMemcpyHostToDevice, hp.h2d);
+    cudaMemcpyAsync(b + off_c, cu_host.data(), cu_host.size() * 4, cudaMemcpyHostToDevice, hp.h2d);
+    const float* d_sinks = sinks ? reinterpret_cast<const float*>(b + off_s) : nullptr;
+    const int32_t* d_cu = reinterpret_cast<const int32_t*>(b + off_c);
+    for (size_t c = 0; c < chunks.size() && st == TSK_OK; ++c) {
+      const HostChunk& ch = chunks[c];
+      const int64_t n = ch.t1 - ch.t0;
+      cudaEvent_t ev_in = event(), ev_out = event();
+      if (!ev_in || !ev_out) {
+        st = cuda_fail(cudaErrorUnknown, "host pipeline events");
+        break;
+      }
+      const uint8_t* hq = static_cast<const uint8_t*>(q) + ch.t0 * qrow;
+      const uint8_t* hk = static_cast<const uint8_t*>(k) + ch.t0 * kvrow;
+      const uint8_t* hv = static_cast<const uint8_t*>(v) + ch.t0 * kvrow;
+      cudaMemcpyAsync(b + off_q + ch.t0 * qrow, hq, n * qrow, cudaMemcpyHostToDevice, hp.h2d);
+      cudaMemcpyAsync(b + off_k + ch.t0 * kvrow, hk, n * kvrow, cudaMemcpyHostToDevice, hp.h2d);
+      cudaMemcpyAsync(b + off_v + ch.t0 * kvrow, hv, n * kvrow, cudaMemcpyHostToDevice, hp.h2d);
+      cudaEventRecord(ev_in, hp.h2d);
+      cudaStream_t cs = hp.comp[c & 1];
+      cudaStreamWaitEvent(cs, ev_in, 0);
+      if (ch.nseq > 0) {
+        st = prefill_impl(b + off_q + ch.t0 * qrow, b + off_k + ch.k0 * kvrow,
+                          b + off_v + ch.k0 * kvrow, d_sinks, d_cu + ch.cu_off,
+                          d_cu + ch.cu_off + ch.nseq + 1, ch.nseq, n, ch.t1 - ch.k0, Hq, Hkv, D,
+                          window, scale, b + off_o + ch.t0 * qrow,
+                          lse ? reinterpret_cast<float*>(b + off_l) + ch.t0 * Hq : nullptr, cs,
+                          "tsk_mha_prefill_host");
+      }
+      cudaEventRecord(ev_out, cs);
+      cudaStreamWaitEvent(hp.d2h, ev_out, 0);
+      cudaMemcpyAsync(static_cast<uint8_t*>(out) + ch.t0 * qrow, b + off_o + ch.t0 * qrow,
+                      n * qrow, cudaMemcpyDeviceToHost, hp.d2h);
+      if (lse)
+        cudaMemcpyAsync(lse + ch.t0 * Hq, b + off_l + ch.t0 * Hq * 4, n * Hq * 4,
+                        cudaMemcpyDeviceToHost, hp.d2h);
+    }
+    // The caller's stream continues once every copy back has finished (the
+    // copy stream waited for both compute streams' chunks).
+    cudaEventRecord(ev_done, hp.d2h);
+    cudaStreamWaitEvent(stream, ev_done, 0);
+    for (cudaStream_t s2 : {hp.h2d, hp.comp[0], hp.comp[1]}) {
+      cudaEvent_t e = event();
+      if (e) {
+        cudaEventRecord(e, s2);
+        cudaStreamWaitEvent(stream, e, 0);
+      }
+    }
+    // Device-side errors of the chunks' kernels (bounded waits) move to the
+    // caller stream's status words, where tsk_get_device_status reads them.
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace* ws = nullptr;
+    if (get_workspace(dev, stream, 1024, 1024, &ws) == TSK_OK) {
+      auto w0 = g_ws.find({dev, hp.comp[0]}), w1 = g_ws.find({dev, hp.comp[1]});
+      int* a0 = w0 != g_ws.end() ? w0->second.base : nullptr;
+      int* a1 = w1 != g_ws.end() ? w1->second.base : nullptr;
+      merge_status_kernel<<<1, 1, 0, stream>>>(ws->base, a0, a1);
+    }
+  }
+  for (cudaEvent_t e : evs) cudaEventDestroy(e);  // released once they complete
+  cudaError_t e = cudaGetLastError();
+  if (st == TSK_OK && e != cudaSuccess) {
+    note_error("tsk_mha_prefill_host", e);
+    st = TSK_ERR_LAUNCH;
+  }
+  return st;
 }

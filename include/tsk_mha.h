@@ -299,6 +299,46 @@ TSK_API tsk_status tsk_mha_prefill_noalloc(const void *q, const void *k, const v
                                            int32_t Hkv, int32_t D, int32_t window, float scale,
                                            void *out, float *lse, tsk_stream_t stream);
 
+/*
+ * tsk_mha_prefill_host -- tsk_mha_prefill with every buffer in host memory:
+ * q, k, v, sinks, cu_seqlens, out and lse are host pointers (same shapes,
+ * types and meaning as for tsk_mha_prefill; cu_seqlens is read on the host,
+ * so all of its checks happen before anything is enqueued and an invalid
+ * array returns TSK_ERR_INVALID_ARG).  The pages define the operation on
+ * device tensors only; this entry point is an addition of this library for
+ * callers whose inputs live in host memory.
+ *
+ * The packed token stream is cut into about eight chunks of consecutive
+ * tokens (at least 2048 each; a chunk ends at a sequence end or at a
+ * multiple of 128 rows from the start of the sequence it cuts, so every
+ * query tile is the one tsk_mha_prefill forms).  Chunk c's attention is a prefill over a
+ * key/value cache: its queries are the chunk's rows, its keys each touched
+ * sequence's rows from the sequence start to the chunk end, all already on
+ * the device.  Copies in (one stream), attention (two streams) and copies
+ * out (one stream) then overlap across chunks; these streams belong to the
+ * library, one set per (device, caller stream).  Results are bit for bit
+ * those of tsk_mha_prefill (the same query tiles visit the same key tiles).
+ *
+ * Asynchronous: the call enqueues work and returns; `stream` continues once
+ * every output byte has reached host memory, so the host buffers must stay
+ * valid (and out/lse unread) until `stream` has passed that point (for
+ * example cudaStreamSynchronize(stream)).  The work starts after everything
+ * enqueued earlier on `stream`.  Copies overlap only with page-locked host
+ * buffers (cudaHostAlloc / cudaHostRegister); with pageable memory the call
+ * still works but the copies serialise the host.  Device memory: a
+ * grow-only buffer of about (2*Hq + 2*Hkv)*D*2 + 4*Hq bytes per token plus the
+ * workspaces of the library's streams, held per (device, caller stream)
+ * until tsk_release.  Device-side errors of the chunks' kernels are reported
+ * by tsk_get_device_status(stream).  Not capturable in a CUDA graph (it
+ * waits on events recorded on its own streams).  Calls on one caller stream
+ * are serialised by a library lock while they enqueue.
+ */
+TSK_API tsk_status tsk_mha_prefill_host(const void *q, const void *k, const void *v,
+                                        const float *sinks, const int32_t *cu_seqlens,
+                                        int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                        int32_t Hkv, int32_t D, int32_t window, float scale,
+                                        void *out, float *lse, tsk_stream_t stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 TSK_API int32_t tsk_version(void);
 

@@ -138,3 +138,36 @@ def test_decode_host_side_rejections(lib, kw, code):
 
 def test_decode_empty_returns_ok(lib):
     assert dec_call(lib, num_seqs=0, total_k=0) == 0
+
+
+def _host_call(lib, cu, num_seqs, total, D=64, Hq=8, Hkv=2, scale=0.125):
+    """tsk_mha_prefill_host with host buffers (numpy) and stream 0."""
+    import numpy as np
+    T = max(int(total), 1)
+    q = np.zeros((T, Hq, D), dtype=np.uint16)
+    kv = np.zeros((T, Hkv, D), dtype=np.uint16)
+    out = np.zeros((T, Hq, D), dtype=np.uint16)
+    cu = np.asarray(cu, dtype=np.int32)
+    return pkg.tsk_mha_prefill_host(q, kv, kv, None, cu, num_seqs, total, Hq, Hkv, D, 0, scale,
+                                    out, None, 0)
+
+
+@pytest.mark.parametrize("cu,n,total,code", [
+    ([1, 5], 1, 5, -1),          # does not start at 0
+    ([0, 5, 3], 2, 3, -1),       # decreasing
+    ([0, 5], 1, 6, -1),          # last offset != total_tokens
+    ([0, 5], -1, 5, -1),         # negative count
+])
+def test_host_buffer_entry_checks_offsets_on_the_host(lib, cu, n, total, code):
+    assert _host_call(lib, cu, n, total) == code
+
+
+def test_host_buffer_entry_rejects_unsupported_shapes(lib):
+    assert _host_call(lib, [0, 5], 1, 5, D=96) == -2
+    assert _host_call(lib, [0, 5], 1, 5, Hq=6, Hkv=4) == -2
+    assert _host_call(lib, [0, 5], 1, 5, scale=float("nan")) == -1
+
+
+def test_host_buffer_entry_empty_returns_ok(lib):
+    assert _host_call(lib, [0], 0, 0) == 0
+    assert _host_call(lib, [0, 0, 0], 2, 0) == 0
