@@ -500,8 +500,7 @@ tsk_status tsk_release(void) {
     cudaDeviceSynchronize();
   for (auto& kv : g_pipe) {
     HostPipe& hp = kv.second;
-    cudaSetDevice(kv.first.first);
-    cudaStreamSynchronize(kv.first.second);
+    cudaSetDevice(kv.first.first);  // (the device was synchronised above)
     if (hp.buf) cudaFree(hp.buf);
     for (cudaStream_t st : {hp.h2d, hp.d2h, hp.comp[0], hp.comp[1]}) {
       auto it = g_ws.find({kv.first.first, st});

@@ -121,3 +121,12 @@ def test_buffer_grows_and_calls_stay_ordered(pkg):
           inputgen.make([1300], 8, 2, seed=66)]
     for w in ws:
         same_as_device(pkg, w, stream=s)
+
+
+def test_release_then_call_again(pkg):
+    """tsk_release frees the pipeline's streams and buffer; the next call
+    creates them again."""
+    w = inputgen.make([2500, 300], 8, 2, seed=67)
+    same_as_device(pkg, w)
+    assert pkg.load_library().tsk_release() == 0
+    same_as_device(pkg, w)
