@@ -1026,6 +1026,12 @@ extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const v
     return TSK_ERR_INVALID_ARG;
   for (int32_t s = 0; s < num_seqs; ++s)
     if (cu_seqlens[s + 1] < cu_seqlens[s]) return TSK_ERR_INVALID_ARG;
+  {
+    const size_t qo = (size_t)total_tokens * Hq * D * 2, kvb = (size_t)total_tokens * Hkv * D * 2;
+    if (total_tokens > 0 && (overlaps(out, qo, q, qo) || overlaps(out, qo, k, kvb) ||
+                             overlaps(out, qo, v, kvb)))
+      return TSK_ERR_INVALID_ARG;
+  }
   if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 

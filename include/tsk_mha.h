@@ -304,7 +304,8 @@ TSK_API tsk_status tsk_mha_prefill_noalloc(const void *q, const void *k, const v
  * q, k, v, sinks, cu_seqlens, out and lse are host pointers (same shapes,
  * types and meaning as for tsk_mha_prefill; cu_seqlens is read on the host,
  * so all of its checks happen before anything is enqueued and an invalid
- * array returns TSK_ERR_INVALID_ARG).  The pages define the operation on
+ * array returns TSK_ERR_INVALID_ARG; so does `out` overlapping q, k or v).
+ * The pages define the operation on
  * device tensors only; this entry point is an addition of this library for
  * callers whose inputs live in host memory.
  *

@@ -171,3 +171,14 @@ def test_host_buffer_entry_rejects_unsupported_shapes(lib):
 def test_host_buffer_entry_empty_returns_ok(lib):
     assert _host_call(lib, [0], 0, 0) == 0
     assert _host_call(lib, [0, 0, 0], 2, 0) == 0
+
+
+def test_host_buffer_entry_rejects_out_overlapping_inputs(lib):
+    import numpy as np
+    T, Hq, Hkv, D = 64, 8, 2, 64
+    q = np.zeros((T, Hq, D), dtype=np.uint16)
+    kv = np.zeros((T, Hkv, D), dtype=np.uint16)
+    cu = np.asarray([0, T], dtype=np.int32)
+    rc = pkg.tsk_mha_prefill_host(q, kv, kv, None, cu, 1, T, Hq, Hkv, D, 0, 0.125,
+                                  q.ctypes.data + 128, None, 0)
+    assert rc == -1
