@@ -4,7 +4,8 @@
 //
 // The work is a stream over the cache (about 4 FLOP per byte for 8 query
 // heads per KV head): the kernels are laid out for HBM bandwidth.
-//   decode_check_kernel   validates cu_seqlens_k (1 CTA)
+//   decode_check_kernel   validates cu_seqlens_k and clears the split counters
+//                         (1 CTA)
 //   decode_split_kernel   one CTA per (key split, KV head, block of <= 16 query
 //                         heads of that KV head, sequence); 4 warps.  One thread
 //                         streams 128-key K and V tiles into a 3-stage
@@ -14,10 +15,11 @@
 //                         of the block are the 16 rows, padded with zeros), with
 //                         an online base-2 softmax per row.  The four warps'
 //                         states are merged in shared memory and the split's
-//                         (m, l, O) written to a workspace.
-//   decode_merge_kernel   one warp per (sequence, query head): combines the
-//                         splits' states and the sink (counted once), writes
-//                         bf16 out and the natural-log LSE.
+//                         (m, l, O) written to a workspace.  The last CTA of a
+//                         (sequence, KV head, head block) to finish (an atomic
+//                         counter per triple) combines the splits' states and
+//                         the sink (counted once) and writes bf16 out and the
+//                         natural-log LSE.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -37,6 +39,7 @@ struct DecParams {
   const float* sinks;       // [Hq] or nullptr
   const int* cu_k;          // [num_seqs + 1]
   float* part;              // [splits][num_seqs][Hq][D + 2]: O (unnormalised), m, l
+  int* counters;            // [num_seqs][Hkv][n_hb]: splits finished (cleared by the check)
   __nv_bfloat16* out;       // [num_seqs, Hq, D]
   float* lse;               // [num_seqs, Hq] or nullptr
   int* status;              // device status words (sticky error code first)
@@ -92,9 +95,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
 
 // cu_k must be 0 = cu_k[0] < cu_k[1] < ... with every length 1 .. max_k and
 // cu_k[num_seqs] = total_k.  Writes this call's verdict to *bad and, on
-// failure, TSK_ERR_BAD_SEQLENS (-8) to the sticky status word.
+// failure, TSK_ERR_BAD_SEQLENS (-8) to the sticky status word.  Also clears
+// the n_counters split counters of this call.
 __global__ void decode_check_kernel(const int* cu_k, int num_seqs, int total_k, int max_k,
-                                    int* status, int* bad_out, PagedKV pg) {
+                                    int* status, int* bad_out, PagedKV pg, int* counters,
+                                    int n_counters) {
+  for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   bool bad = false;
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
     const int a = cu_k[s], b = cu_k[s + 1];
@@ -342,39 +348,53 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
   }
-}
 
-// One warp per (sequence, query head): combine the splits and the sink.
-template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecParams p) {
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (gw >= p.num_seqs * p.Hq) return;
-  if (*reinterpret_cast<const volatile int*>(p.bad) != 0) return;
-  const int b = gw / p.Hq, h = gw - b * p.Hq;
-  const float sink2 = p.sinks ? p.sinks[h] * 1.4426950408889634f : -INFINITY;
-  float M = sink2;
-  for (int s = 0; s < p.splits; ++s)
-    M = fmaxf(M, p.part[(((size_t)s * p.num_seqs + b) * p.Hq + h) * (D + 2) + D]);
-  float Z = p.sinks ? ex2_approx(sink2 - M) : 0.f;
-  constexpr int per = D / 32;
-  float acc[per];
-#pragma unroll
-  for (int j = 0; j < per; ++j) acc[j] = 0.f;
-  for (int s = 0; s < p.splits; ++s) {
-    const float* src = p.part + (((size_t)s * p.num_seqs + b) * p.Hq + h) * (D + 2);
-    const float ms = src[D];
-    if (ms == -INFINITY) continue;
-    const float wgt = ex2_approx(ms - M);
-    Z += wgt * src[D + 1];
-#pragma unroll
-    for (int j = 0; j < per; ++j) acc[j] += wgt * src[lane * per + j];
+  // The last CTA of this (sequence, KV head, head block) to get here merges
+  // the splits (release: each CTA's partial writes are fenced before its
+  // count; acquire: the last one fences after it and reads around L1).
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int prev = atomicAdd(p.counters + ((size_t)b * p.Hkv + g) * p.n_hb + hb, 1);
+    s_last = prev == p.splits - 1;
+    if (s_last) __threadfence();
   }
-  const float inv = 1.f / Z;
-  __nv_bfloat16* o = p.out + ((size_t)b * p.Hq + h) * D + lane * per;
+  __syncthreads();
+  if (!s_last) return;
+  {
+    // 128 threads: eight per query head of the block, D / 8 columns each.
+    const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
+    constexpr int per = D / 8;
+    if (r < rows) {
+      const int h = g * p.G + h_lo + r;
+      const float sink2 = p.sinks ? p.sinks[h] * 1.4426950408889634f : -INFINITY;
+      auto src_of = [&](int sp) {
+        return p.part + (((size_t)sp * p.num_seqs + b) * p.Hq + h) * (D + 2);
+      };
+      float M = sink2;
+      for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, __ldcg(src_of(sp) + D));
+      float Z = p.sinks ? ex2_approx(sink2 - M) : 0.f;
+      float acc[per];
 #pragma unroll
-  for (int j = 0; j < per; j += 2)
-    *reinterpret_cast<uint32_t*>(o + j) = pack_bf16x2(acc[j] * inv, acc[j + 1] * inv);
-  if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + h] = (M + log2f(Z)) * 0.69314718055994531f;
+      for (int j = 0; j < per; ++j) acc[j] = 0.f;
+      for (int sp = 0; sp < p.splits; ++sp) {
+        const float* src = src_of(sp);
+        const float ms = __ldcg(src + D);
+        if (ms == -INFINITY) continue;
+        const float wgt = ex2_approx(ms - M);
+        Z += wgt * __ldcg(src + D + 1);
+#pragma unroll
+        for (int j = 0; j < per; ++j) acc[j] += wgt * __ldcg(src + part * per + j);
+      }
+      const float inv = 1.f / Z;
+      __nv_bfloat16* o = p.out + ((size_t)b * p.Hq + h) * D + part * per;
+#pragma unroll
+      for (int j = 0; j < per; j += 2)
+        *reinterpret_cast<uint32_t*>(o + j) = pack_bf16x2(acc[j] * inv, acc[j + 1] * inv);
+      if (p.lse && part == 0) p.lse[(size_t)b * p.Hq + h] = (M + log2f(Z)) * 0.69314718055994531f;
+    }
+  }
 }
 
 }  // namespace dec

@@ -730,7 +730,10 @@ tsk_status decode_impl(const void* q, const void* k, const void* v, const float*
     }
   }
 
-  const size_t need = (size_t)splits * num_seqs * Hq * (D + 2) * sizeof(float);
+  // Partial states, then one split counter per (sequence, KV head, head block).
+  const size_t part_floats = (size_t)splits * num_seqs * Hq * (D + 2);
+  const int n_counters = num_seqs * Hkv * n_hb;
+  const size_t need = part_floats * sizeof(float) + (size_t)n_counters * sizeof(int);
   if (ws->part_bytes < need) {
     float* nb = nullptr;
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), need, stream);
@@ -749,6 +752,7 @@ tsk_status decode_impl(const void* q, const void* k, const void* v, const float*
   p.sinks = sinks;
   p.cu_k = cu_seqlens_k;
   p.part = ws->part;
+  p.counters = reinterpret_cast<int*>(ws->part + part_floats);
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = ws->base + tsk::kWsStatus;
@@ -787,17 +791,14 @@ tsk_status decode_impl(const void* q, const void* k, const void* v, const float*
   }
   tsk::dec::decode_check_kernel<<<1, 1024, 0, stream>>>(cu_seqlens_k, num_seqs, (int)total_k,
                                                        max_seqlen_k, ws->base + tsk::kWsStatus,
-                                                       ws->base + tsk::kWsDecodeBad, pg);
+                                                       ws->base + tsk::kWsDecodeBad, pg,
+                                                       p.counters, n_counters);
   if (prof) cudaEventRecord(g_ev[1], stream);
   const dim3 grid(splits, Hkv * n_hb, num_seqs);
-  const int mgrid = (int)(((int64_t)num_seqs * Hq * 32 + 255) / 256);
-  if (D == 64) {
+  if (D == 64)
     tsk::dec::decode_split_kernel<64><<<grid, tsk::dec::kThreads, tsk::dec::smem_bytes<64>(), stream>>>(tk, tv, p);
-    tsk::dec::decode_merge_kernel<64><<<mgrid, 256, 0, stream>>>(p);
-  } else {
+  else
     tsk::dec::decode_split_kernel<128><<<grid, tsk::dec::kThreads, tsk::dec::smem_bytes<128>(), stream>>>(tk, tv, p);
-    tsk::dec::decode_merge_kernel<128><<<mgrid, 256, 0, stream>>>(p);
-  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) note_error("decode kernel launch", e);
   if (prof) {

@@ -130,8 +130,10 @@ TSK_API tsk_status tsk_mha_prefill_kvcache(const void *q, const void *k, const v
  * positions max(0, Lk - W) .. Lk - 1 (all of them for W <= 0), with the sink
  * of its head counted once.  Identical to tsk_mha_prefill_kvcache with one
  * query per sequence.  The keys of a sequence are split over several CTAs
- * when the batch alone would not fill the GPU; the splits' partial softmax
- * states are merged by a second kernel.
+ * when the batch alone would not fill the GPU; the last CTA of each
+ * (sequence, KV head, block of query heads) to finish merges the splits'
+ * partial softmax states.  Two launches: an offset check, then the split
+ * kernel.
  *
  *   q             device, bf16 [num_seqs, Hq, D]
  *   k, v          device, bf16 [total_k, Hkv, D] (contiguous per sequence)
@@ -146,7 +148,8 @@ TSK_API tsk_status tsk_mha_prefill_kvcache(const void *q, const void *k, const v
  * length above max_seqlen_k are reported as TSK_ERR_BAD_SEQLENS through
  * tsk_get_device_status and nothing is written.  Limits: num_seqs <= 65535,
  * total_k * Hkv < 2^31.  The library keeps a per-(device, stream) buffer of
- * splits x num_seqs x Hq x (D + 2) floats for the partial states.
+ * splits x num_seqs x Hq x (D + 2) floats for the partial states and one int
+ * counter per (sequence, KV head, block of 16 query heads).
  */
 TSK_API tsk_status tsk_mha_decode_kvcache(const void *q, const void *k, const void *v,
                                          const float *sinks, const int32_t *cu_seqlens_k,
