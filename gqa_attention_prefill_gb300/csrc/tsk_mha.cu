@@ -710,21 +710,23 @@ tsk_status decode_impl(const void* q, const void* k, const void* v, const float*
   const int span = windowed ? window : max_seqlen_k;
   const int n_tiles = (span + tsk::dec::kKeys - 1) / tsk::dec::kKeys + (windowed ? 1 : 0);
   // Among split counts from the smallest that gives two waves to four times
-  // that, take the one whose last wave is fullest (fewest splits on ties).
+  // that, take the one with the least estimated time: waves of resident CTAs
+  // x (tiles per CTA + 2), the 2 standing for a CTA's fixed cost (ring fill,
+  // state merge, partial write) in tile loads (fewest splits on ties).
   const int64_t base_ctas = (int64_t)num_seqs * Hkv * n_hb;
   const int64_t slots = (int64_t)ds->num_sms * (D == 64 ? 2 : 1);  // resident CTAs
   int s_lo = (int)((2 * slots + base_ctas - 1) / base_ctas);
   s_lo = s_lo < 1 ? 1 : (s_lo > n_tiles ? n_tiles : s_lo);
   const int s_hi = 4 * s_lo < n_tiles ? 4 * s_lo : n_tiles;
   int splits = s_lo, tps = (n_tiles + s_lo - 1) / s_lo;
-  double best = -1.0;
+  double best = 1e300;
   for (int c = s_lo; c <= s_hi; ++c) {
     const int t = (n_tiles + c - 1) / c;
     const int sc = (n_tiles + t - 1) / t;  // splits that tile count really needs
-    const int64_t ctas = base_ctas * sc;
-    const double eff = (double)ctas / (double)(((ctas + slots - 1) / slots) * slots);
-    if (eff > best + 1e-9) {
-      best = eff;
+    const int64_t waves = (base_ctas * sc + slots - 1) / slots;
+    const double cost = (double)waves * (t + 2);
+    if (cost < best - 1e-9) {
+      best = cost;
       splits = sc;
       tps = t;
     }
