@@ -4,7 +4,11 @@
 // list, which the scheduler pre-pass sorted by cost (longest first).  A unit
 // is (query tile of 128 rows, KV head g, head pair): two query heads of the
 // same KV group over the same 128 tokens, so both share every K/V tile staged
-// in shared memory (GQA reuse) and have identical key ranges.  Roles:
+// in shared memory (GQA reuse) and have identical key ranges.  With one query
+// head per KV head (Hq == Hkv) a unit is instead two consecutive 128-row
+// tiles of one head (list entries of 256 rows, key range the union of the
+// two; a key tile only one tile needs is fully masked for the other and adds
+// exact zeros), so that both query tiles of the CTA stay busy.  Roles:
 //   warp 0        TMA producer: Q tiles (2 x 16 KB, double buffered) and a
 //                 ring of kStages K/V stages (16 KB + 16 KB each)
 //   warp 1        allocates TMEM; one lane issues tile 0's tcgen05.mma:
@@ -112,6 +116,10 @@ struct Unit {
   int seq;      // sequence index (block-table row of a paged cache)
 };
 
+// Unit u.  QS (a kernel template parameter) is the row offset between the
+// unit's two query tiles: 0 when they are two heads over the same rows,
+// kTileM when they are two row blocks of one head (Hq == Hkv).
+template <int QS = 0>
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   const int per_tile = p.Hkv * p.HP;
   const int qi = u / per_tile;
@@ -130,8 +138,18 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   r.g = rem / p.HP;
   const int hp = rem - r.g * p.HP;
   r.h0 = r.g * p.G + 2 * hp;
-  r.ntiles = (2 * hp + 1 < p.G) ? 2 : 1;
+  r.ntiles = QS ? (r.q0 + QS < r.len ? 2 : 1) : ((2 * hp + 1 < p.G) ? 2 : 1);
   return r;
+}
+
+// Query head and first query row (relative to the sequence) of tile t of a unit.
+template <int QS>
+__device__ __forceinline__ int tile_head(const Unit& w, int t) {
+  return w.h0 + (QS ? 0 : t);
+}
+template <int QS>
+__device__ __forceinline__ int tile_q0(const Unit& w, int t) {
+  return w.q0 + t * QS;
 }
 
 // The unit's sequence fields read again (volatile loads: not merged with the
@@ -187,6 +205,7 @@ struct Ctx {
 
 
 // TMA producer (one thread).
+template <int QS>
 __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* tmQ,
                                            const CUtensorMap* tmK, const CUtensorMap* tmV,
                                            const AttnParams& p) {
@@ -195,14 +214,14 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   bool ok = true;
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<QS>(p, u);
     const int qb = q_iter & 1;
     if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, 1, p, cx.abort);
     if (!ok) break;
     mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), w.ntiles * kTileBytes);
     for (int t = 0; t < w.ntiles; ++t)
       tma_load_3d(cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes, tmQ, cx.bar(kBarQFull + qb), 0,
-                  w.h0 + t, w.start + w.q0);
+                  tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t));
     ++q_iter;
     for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
       const int s = kv_iter % kStages;
@@ -239,6 +258,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
 // Each issuer releases a K/V stage (and the Q buffer) with its own commit, so
 // those barriers count two arrivals; for a unit with one query tile the tile-0
 // issuer commits twice and the tile-1 issuer only advances its counters.
+template <int QS>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
   bool ok = true;
@@ -246,7 +266,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
   const uint32_t a_p = cx.tmem + kColP0 + 64 * t;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<QS>(p, u);
     const int qb = q_iter & 1;
     if (t >= w.ntiles) {  // this tile is idle in the unit
       kv_iter += w.n_kv;
@@ -343,6 +363,7 @@ __device__ __forceinline__ ChunkMask classify_chunks(int row0, int kbase, int wi
 // each row's 128 scores are held in registers for one pass (maximum, then
 // exponentials), edge tiles are masked per element, and each thread stores
 // its output row directly.
+template <int QS>
 __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnParams& p,
                                                     const CUtensorMap* tmO, int warp, int lane) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
@@ -364,14 +385,14 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     int n_kv, kv_lo, diag0, pos;
     float m_used = -INFINITY, l = 0.f;
     {
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit<QS>(p, u);
       if (t >= w.ntiles) continue;
       n_kv = w.n_kv;
       kv_lo = w.kv_lo;
-      diag0 = w.offset + w.q0;  // key position of the tile's first query row
-      pos = diag0 + r;          // key position of this thread's query row
+      diag0 = w.offset + tile_q0<QS>(w, t);  // key position of the tile's first query row
+      pos = diag0 + r;                      // key position of this thread's query row
       if (p.sinks) {
-        m_used = __ldg(p.sinks + w.h0 + t) * 1.4426950408889634f;
+        m_used = __ldg(p.sinks + tile_head<QS>(w, t)) * 1.4426950408889634f;
         l = 1.f;
       }
     }
@@ -491,9 +512,15 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     // ------------------------------------------------------------ epilogue
     const int per_tile = p.Hkv * p.HP;
     const int qi = u / per_tile;
-    const int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
+    int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
     const int g = (u - qi * per_tile) / p.HP;
-    const int h = g * p.G + 2 * (u - qi * per_tile - g * p.HP) + t;
+    int h;
+    if constexpr (QS != 0) {
+      h = g * p.G;
+      e.y += t * QS;  // first query row of this tile
+    } else {
+      h = g * p.G + 2 * (u - qi * per_tile - g * p.HP) + t;
+    }
     ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
     TSK_TRACE_T0(tr_epi);
     if (!ok) break;
@@ -551,6 +578,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
 // stores the slice with one TMA bulk tensor store (box 64 x 1 x 32).  Warps
 // whose rows run past the end of their sequence (rows beyond it belong to the
 // next sequence) use direct per-row stores instead.
+template <int QS>
 __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnParams& p,
                                                     const CUtensorMap* tmO, int warp, int lane) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
@@ -566,11 +594,12 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
   TSK_TRACE_T0(tr_all);
   bool ok = true;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<QS>(p, u);
     if (t >= w.ntiles) continue;
-    const int h = w.h0 + t;
-    const int row = w.q0 + r;        // query row, relative to the sequence's first query
-    const int pos = w.offset + row;  // its key position
+    const int h = tile_head<QS>(w, t);
+    const int q0t = tile_q0<QS>(w, t);  // first query row of this tile
+    const int row = q0t + r;           // query row, relative to the sequence's first query
+    const int pos = w.offset + row;    // its key position
     float m_used = -INFINITY, l = 0.f;
     if (p.sinks) {
       m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
@@ -583,10 +612,10 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       ++s_cnt;
       tc_fence_after();
       const int kbase = kt * kTileN;
-      const bool edge = (kbase + kTileN - 1 > w.offset + w.q0) ||
-                        (p.window > 0 && kbase < w.offset + w.q0 + kTileM - p.window);
+      const bool edge = (kbase + kTileN - 1 > w.offset + q0t) ||
+                        (p.window > 0 && kbase < w.offset + q0t + kTileM - p.window);
       ChunkMask cm{0u, 0u};
-      if (edge) cm = classify_chunks(w.offset + w.q0 + wq * 32, kbase, p.window);
+      if (edge) cm = classify_chunks(w.offset + q0t + wq * 32, kbase, p.window);
       const int hi_c = pos - kbase;
       const int lo_c = p.window > 0 ? pos - p.window + 1 - kbase : -1;
       // The row's 128 scores are processed as two halves of 64 columns, so
@@ -733,7 +762,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
     const size_t orow = (size_t)(w.start + row) * p.Hq + h;
     if (p.lse && row < w.len) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
-    if (w.q0 + wq * 32 + 32 <= w.len) {
+    if (q0t + wq * 32 + 32 <= w.len) {
       // The warp's 32 rows lie inside the sequence: stage them in this warp's
       // slice of the staging tile and store them with one TMA bulk store.
       if (lane == 0) bulk_wait_group_read0();  // the warp's previous store has read its slice
@@ -746,7 +775,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, w.start + w.q0 + wq * 32);
+        tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, w.start + q0t + wq * 32);
         bulk_commit_group();
       }
     } else if (row < w.len) {
@@ -764,7 +793,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
 // kSmallWindow selects the softmax role for 0 < window <= kSmallWindowMax.
 constexpr int kSmallWindowMax = 512;
 
-template <bool kSmallWindow>
+template <bool kSmallWindow, int QS>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -822,12 +851,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   cx.abort = smem_u32(const_cast<int*>(abort_flag));
   cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
 
-  if (warp == 0 && lane == 0) role_producer(cx, &tmQ, &tmK, &tmV, p);
-  else if (warp == 1 && lane == 0) role_mma(cx, p, 0);
-  else if (warp == 2 && lane == 0) role_mma(cx, p, 1);
+  if (warp == 0 && lane == 0) role_producer<QS>(cx, &tmQ, &tmK, &tmV, p);
+  else if (warp == 1 && lane == 0) role_mma<QS>(cx, p, 0);
+  else if (warp == 2 && lane == 0) role_mma<QS>(cx, p, 1);
   else if (warp >= kFirstSoftmaxWarp) {
-    if constexpr (kSmallWindow) role_softmax_window(cx, p, &tmO, warp, lane);
-    else role_softmax_causal(cx, p, &tmO, warp, lane);
+    if constexpr (kSmallWindow) role_softmax_window<QS>(cx, p, &tmO, warp, lane);
+    else role_softmax_causal<QS>(cx, p, &tmO, warp, lane);
   }
 
   // ------------------------------------------------------------------ teardown

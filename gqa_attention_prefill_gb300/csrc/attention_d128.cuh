@@ -74,6 +74,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo)
 }
 
 // TMA producer (one thread).
+template <int QS>
 __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* tmQ,
                                               const CUtensorMap* tmK, const CUtensorMap* tmV,
                                               const AttnParams& p) {
@@ -82,14 +83,14 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   TSK_TL_DECL;
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<QS>(p, u);
     if (q_iter >= 1) ok = mbar_wait(cx.bar(kBarQEmpty), (q_iter - 1) & 1, 1, p, cx.abort);
     if (!ok) break;
     mbar_arrive_expect_tx(cx.bar(kBarQFull), w.ntiles * kTile);
     for (int t = 0; t < w.ntiles; ++t)
       for (int hf = 0; hf < 2; ++hf)
         tma_load_3d(cx.sbase + kSmemQ + t * kTile + hf * kHalf, tmQ, cx.bar(kBarQFull), 64 * hf,
-                    w.h0 + t, w.start + w.q0);
+                    tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t));
     TSK_EV(20);
     ++q_iter;
     for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -134,6 +135,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
 // tcgen05.mma issuer for query tile t (one thread).  The release barriers
 // (Q, K and V buffers) count one arrival per tile; for a unit with a single
 // query tile, tile 0 arrives twice.
+template <int QS>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, p_cnt = 0;
   bool ok = true;
@@ -143,7 +145,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   const uint32_t a_p = d_s + kColP;
   const uint32_t q_addr = cx.sbase + kSmemQ + t * kTile;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<QS>(p, u);
     if (t >= w.ntiles) {
       kv_iter += w.n_kv;
       ++q_iter;
@@ -212,6 +214,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
 }
 
 // Softmax and epilogue of query tile t (one warpgroup, one thread per row).
+template <int QS>
 __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
                                              const CUtensorMap* tmO, int warp, int lane) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;
@@ -232,15 +235,15 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
     bool pair;  // two query tiles: their softmax steps alternate
     float m_used = -INFINITY, l = 0.f;
     {
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit<QS>(p, u);
       if (t >= w.ntiles) continue;
       pair = w.ntiles == 2;
       n_kv = w.n_kv;
       kv_lo = w.kv_lo;
-      diag0 = w.offset + w.q0;
+      diag0 = w.offset + tile_q0<QS>(w, t);
       pos = diag0 + r;
       if (p.sinks) {
-        m_used = __ldg(p.sinks + w.h0 + t) * 1.4426950408889634f;
+        m_used = __ldg(p.sinks + tile_head<QS>(w, t)) * 1.4426950408889634f;
         l = 1.f;
       }
     }
@@ -358,9 +361,15 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
     // ------------------------------------------------------------ epilogue
     const int per_tile = p.Hkv * p.HP;
     const int qi = u / per_tile;
-    const int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
+    int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
     const int g = (u - qi * per_tile) / p.HP;
-    const int h = g * p.G + 2 * (u - qi * per_tile - g * p.HP) + t;
+    int h;
+    if constexpr (QS != 0) {
+      h = g * p.G;
+      e.y += t * QS;  // first query row of this tile
+    } else {
+      h = g * p.G + 2 * (u - qi * per_tile - g * p.HP) + t;
+    }
     ok = mbar_wait_warp(cx.bar(kBarODone + t), o_cnt & 1, 25, p, cx.abort);
     if (!ok) break;
     ++o_cnt;
@@ -411,6 +420,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
   if (lane == 0) bulk_wait_group0();  // every output store of this warp has completed
 }
 
+template <int QS>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ,
                               const __grid_constant__ CUtensorMap tmK,
@@ -475,12 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // between neighbouring splits.)
   if (warp < kFirstSoftmaxWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
-    if (warp == 0 && lane == 0) d128::role_producer(cx, &tmQ, &tmK, &tmV, p);
-    else if (warp == 1 && lane == 0) d128::role_mma(cx, p, 0);
-    else if (warp == 2 && lane == 0) d128::role_mma(cx, p, 1);
+    if (warp == 0 && lane == 0) d128::role_producer<QS>(cx, &tmQ, &tmK, &tmV, p);
+    else if (warp == 1 && lane == 0) d128::role_mma<QS>(cx, p, 0);
+    else if (warp == 2 && lane == 0) d128::role_mma<QS>(cx, p, 1);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
-    d128::role_softmax(cx, p, &tmO, warp, lane);
+    d128::role_softmax<QS>(cx, p, &tmO, warp, lane);
   }
 
   __syncwarp();

@@ -1,6 +1,7 @@
 // Varlen scheduler pre-pass: one CTA turns the sequence offsets into the list
-// of query tiles (128 query rows of one sequence), each with its key-tile
-// range, sorted by cost (number of key tiles) in descending order, so that
+// of query tiles (entry_rows = 128 query rows of one sequence, or 256 when a
+// work unit takes two consecutive 128-row tiles of one head), each with its
+// key-tile range, sorted by cost (number of key tiles) in descending order, so that
 // the persistent attention kernel hands out the longest work first
 // (longest-processing-time order).  Sequence s has Lq = cu[s+1] - cu[s]
 // queries and Lk = cu_k[s+1] - cu_k[s] >= Lq keys; query i sits at key
@@ -29,9 +30,10 @@ constexpr int kWsHeader = 8;   // ints; tile offsets follow, then the int4 list 
 //   {start_k, offset, n_kv, 0}   key start row, Lk - Lq, number of key tiles
 constexpr int kTileEntryInts = 8;
 
-// Key tiles [kv_lo, kv_lo + n_kv) a query tile starting at q0 needs.
-__device__ __forceinline__ int2 qtile_key_range(int q0, int len_q, int offset, int window) {
-  const int last = (q0 + kTileM - 1 < len_q - 1 ? q0 + kTileM - 1 : len_q - 1);
+// Key tiles [kv_lo, kv_lo + n_kv) the `rows` query rows starting at q0 need.
+__device__ __forceinline__ int2 qtile_key_range(int q0, int len_q, int offset, int window,
+                                                int rows = kTileM) {
+  const int last = (q0 + rows - 1 < len_q - 1 ? q0 + rows - 1 : len_q - 1);
   const int kv_hi = (offset + last) / kTileN;
   int kv_lo = 0;
   if (window > 0) {
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k,
                     int num_seqs, int total_tokens, int total_keys, int window,
                     int* __restrict__ ws, int* __restrict__ tile_off, int4* __restrict__ list,
-                    int max_tiles, PagedKV pg) {
+                    int max_tiles, PagedKV pg, int entry_rows) {
   __shared__ int s_scan[kSchedThreads];
   __shared__ int s_hist[kCostBins];
   __shared__ int s_cursor[kCostBins];
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
         s_bad = 1;
         L = 0;
       }
-      nt = (L + kTileM - 1) / kTileM;
+      nt = (L + entry_rows - 1) / entry_rows;
     }
     s_scan[tid] = nt;
     __syncthreads();
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     int qt = i - tile_off[s];
     const int len = cu[s + 1] - cu[s];
     const int cost =
-        qtile_key_range(qt * kTileM, len, (cu_k[s + 1] - cu_k[s]) - len, window).y;
+        qtile_key_range(qt * entry_rows, len, (cu_k[s + 1] - cu_k[s]) - len, window, entry_rows).y;
     atomicAdd(&s_hist[min(cost, kCostBins) - 1], 1);
   }
   __syncthreads();
@@ -169,10 +171,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   for (int i = tid; i < n_tiles; i += kSchedThreads) {
     int s = seq_of(i);
     int qt = i - tile_off[s];
-    const int q0 = qt * kTileM;
+    const int q0 = qt * entry_rows;
     const int len = cu[s + 1] - cu[s];
     const int offset = (cu_k[s + 1] - cu_k[s]) - len;
-    const int2 kr = qtile_key_range(q0, len, offset, window);
+    const int2 kr = qtile_key_range(q0, len, offset, window, entry_rows);
     const int pos = atomicAdd(&s_cursor[min(kr.y, kCostBins) - 1], 1);
     list[2 * pos] = make_int4(cu[s], q0, kr.x, len);
     list[2 * pos + 1] = make_int4(cu_k[s], offset, kr.y, s);

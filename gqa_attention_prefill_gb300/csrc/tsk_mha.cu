@@ -141,15 +141,28 @@ tsk_status check_device(int* dev_out, DeviceState** st_out) {
   }
   if (!st.supported) return TSK_ERR_DEVICE;
   if (!st.smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<false>,
+    constexpr int kQS = tsk::kTileM;  // units of two row blocks of one head
+    cudaError_t e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<false, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tsk::kSmemBytesCausal);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<true>,
+      e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<true, 0>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::kSmemBytesWindow);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel,
+      e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<false, kQS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::kSmemBytesCausal);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::attention_fwd_kernel<true, kQS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::kSmemBytesWindow);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel<0>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::d128::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel<kQS>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::d128::kSmemBytes);
     if (e == cudaSuccess)
@@ -275,19 +288,28 @@ int32_t tsk_kernels_per_call(void) { return 2; }
 
 namespace {
 
-// The attention kernel for head dimension D (64 or 128) and the window.
-void launch_attention(int D, int window, int grid, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, const CUtensorMap& to, const tsk::AttnParams& p,
-                      cudaStream_t stream) {
+// The attention kernel for head dimension D (64 or 128), the window and the
+// unit layout (qstep: 0 = two heads of a group over the same rows, kTileM =
+// two row blocks of one head).
+template <int QS>
+void launch_attention_qs(int D, int window, int grid, const CUtensorMap& tq,
+                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                         const tsk::AttnParams& p, cudaStream_t stream) {
   if (D == 128)
-    tsk::d128::attention_fwd_d128_kernel<<<grid, tsk::kThreads, tsk::d128::kSmemBytes, stream>>>(
-        tq, tk, tv, to, p);
+    tsk::d128::attention_fwd_d128_kernel<QS>
+        <<<grid, tsk::kThreads, tsk::d128::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   else if (window > 0 && window <= tsk::kSmallWindowMax)
-    tsk::attention_fwd_kernel<true><<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(
-        tq, tk, tv, to, p);
+    tsk::attention_fwd_kernel<true, QS>
+        <<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(tq, tk, tv, to, p);
   else
-    tsk::attention_fwd_kernel<false><<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(
-        tq, tk, tv, to, p);
+    tsk::attention_fwd_kernel<false, QS>
+        <<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(tq, tk, tv, to, p);
+}
+void launch_attention(int D, int window, int qstep, int grid, const CUtensorMap& tq,
+                      const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                      const tsk::AttnParams& p, cudaStream_t stream) {
+  if (qstep) launch_attention_qs<tsk::kTileM>(D, window, grid, tq, tk, tv, to, p, stream);
+  else launch_attention_qs<0>(D, window, grid, tq, tk, tv, to, p, stream);
 }
 
 // Shared by tsk_mha_prefill (cu_k == cu_q, total_keys == total_queries) and
@@ -383,9 +405,12 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
     }
     cudaEventRecord(g_ev[0], stream);
   }
+  // With one query head per KV head, a unit takes two consecutive 128-row
+  // tiles of one head (list entries of 256 rows); else two heads of a group.
+  const int qstep = Hq == Hkv ? tsk::kTileM : 0;
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
       cu_q, cu_k, num_seqs, (int)total_q, (int)total_k, window, ws->base, tile_off, list,
-      ws->max_tiles, pg);
+      ws->max_tiles, pg, tsk::kTileM + qstep);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
   tsk::AttnParams p;
@@ -406,7 +431,7 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   p.kv = pg;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  launch_attention(D, window, grid, tq, tk, tv, to, p, stream);
+  launch_attention(D, window, qstep, grid, tq, tk, tv, to, p, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) note_error("attention kernel launch", e);
   if (prof) {
@@ -624,9 +649,10 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   // tile count must start at zero.
   cudaError_t e = cudaMemsetAsync(scratch, 0, tsk::kWsHeader * sizeof(int), stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch header");
+  const int qstep = Hq == Hkv ? tsk::kTileM : 0;  // see prefill_impl
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, scratch,
-      tile_off, list, kNoAllocMaxTiles, tsk::PagedKV{nullptr, 0, 0, 0});
+      tile_off, list, kNoAllocMaxTiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM + qstep);
 
   tsk::AttnParams p;
   p.sinks = sinks;
@@ -646,7 +672,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  launch_attention(D, window, grid, tq, tk, tv, to, p, stream);
+  launch_attention(D, window, qstep, grid, tq, tk, tv, to, p, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     note_error("attention kernel launch (no-alloc)", e);
@@ -937,7 +963,7 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   }
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, ws->base,
-      tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0});
+      tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM);
   tsk::fp8::fp8_vt_kernel<<<dim3(max_tiles, Hkv), 128, 0, stream>>>(
       reinterpret_cast<const uint8_t*>(v8), cu_seqlens, tile_off, ws->base, num_seqs, Hkv, ws->vt,
       t_pad);

@@ -292,6 +292,10 @@ CONFIGS = {
                                            "sinks N(0,1), scale 1/sqrt(128), full causal"),
     "long_1x32768_h32kv8_d128": dict(desc="1 seq x 32768 tokens, Hq=32, Hkv=8, D=128, "
                                           "K = bf16(3*N(0,1)), scale 1/sqrt(128), full causal"),
+    # other query-head group sizes G = Hq / Hkv (1: plain multi-head attention)
+    "causal_4x4096_h32kv32_d128": dict(desc="as causal_4x4096_h32kv8_d128 with Hkv=32 (G=1)"),
+    "causal_4x4096_h64kv8_d128": dict(desc="as causal_4x4096_h32kv8_d128 with Hq=64 (G=8)"),
+    "causal_4x4096_h64kv64": dict(desc="as causal_4x4096_h64kv8 with Hkv=64 (G=1)"),
 }
 
 
@@ -325,6 +329,12 @@ def config(name: str, seed: int = 0) -> Workload:
         return make([4096] * 4, 32, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
     if name == "long_1x32768_h32kv8_d128":
         return make([32768], 32, 8, D=128, scale=128 ** -0.5, k_mult=3.0, seed=seed, name=name)
+    if name == "causal_4x4096_h32kv32_d128":
+        return make([4096] * 4, 32, 32, D=128, scale=128 ** -0.5, seed=seed, name=name)
+    if name == "causal_4x4096_h64kv8_d128":
+        return make([4096] * 4, 64, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
+    if name == "causal_4x4096_h64kv64":
+        return make([4096] * 4, 64, 64, seed=seed, name=name)
     raise KeyError(name)
 
 

@@ -87,6 +87,15 @@ def test_matches_device_entry_point(pkg, seqlens, window):
     same_as_device(pkg, w)
 
 
+def test_one_query_head_per_kv_head(pkg):
+    """Hq == Hkv: units of two row blocks of one head, chunks ending on odd
+    128-row boundaries."""
+    w = inputgen.make([3000, 0, 5000, 129, 7000], 4, 4, seed=68)
+    same_as_device(pkg, w)
+    w = inputgen.make([9000, 3000], 4, 4, D=128, window=300, scale=128 ** -0.5, seed=69)
+    same_as_device(pkg, w)
+
+
 def test_head_dim_128_and_no_sinks_no_lse(pkg):
     w = inputgen.make([5000, 9000, 3], 8, 2, D=128, window=0, seed=61)
     same_as_device(pkg, w)
