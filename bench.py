@@ -465,7 +465,9 @@ def main():
                 "via": ("tsk_mha_prefill_host (pinned host buffers; chunked copies overlapped "
                         "with the attention)" if host_api else
                         "pinned host buffers copied by torch, then the device entry point")},
-        "gpu_launches": args.steps * (2 if decode else pkg.tsk_kernels_per_call()),
+        # decode: offset check + split kernel; FP8: scheduler + V transpose +
+        # attention; otherwise tsk_mha_prefill's scheduler + attention
+        "gpu_launches": args.steps * (2 if decode else 3 if fp8 else pkg.tsk_kernels_per_call()),
         "clocks": clk.summary(),
         "kernel_source_hash": kernel_source_hash(D, decode, fp8),
     }
