@@ -151,7 +151,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_rate(w, seconds_target, seed_stream=77):
+def oracle_rate(w, seconds_target, seed_stream=77, keep=None):
     """Times the CPU oracle on a uniform sample of (token, head) rows of `w`
     sized for about `seconds_target` of CPU work.  Returns (flop/s, rows,
     seconds, threads, flops)."""
@@ -179,8 +179,10 @@ def oracle_rate(w, seconds_target, seed_stream=77):
     n2 = int(min(4_000_000, max(n, n * seconds_target / max(dt, 1e-3))))
     t, h, fl = rows_flops(n2)
     t0 = time.perf_counter()
-    _, _, thr = oracle.run_workload(w, rows=(t, h))
+    ro, rl, thr = oracle.run_workload(w, rows=(t, h))
     dt = time.perf_counter() - t0
+    if keep is not None:   # the sampled rows and the oracle's values for them
+        keep.update(t=t, h=h, out=ro, lse=rl)
     return fl / dt, n2, dt, thr, fl
 
 
@@ -207,6 +209,57 @@ def barrier(ws):
         dist.barrier()
 
 
+def roofline_of(flops, alg_bytes, kernel_s, peaks, peak_src, fp8=False):
+    """The tensor-core and HBM roofs of one launch (algorithmic FLOP and bytes
+    over the kernel time), and the binding one: HBM when the arithmetic
+    intensity is below the ridge point (peak FLOP/s over peak bytes/s), the
+    tensor cores above it."""
+    # E4M3 contractions: twice the dense bf16 rate (the nominal fp8/bf16 ratio)
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    roofs = {
+        "tensor": {"achieved": flops / kernel_s / 1e12, "peak": tensor_peak, "unit": "TFLOP/s",
+                   "frac": flops / kernel_s / 1e12 / tensor_peak,
+                   "peak_source": (f"{peak_src} dense bf16 (burst) x 2 for E4M3" if fp8 else
+                                   f"{peak_src} dense bf16 (burst)")},
+        "hbm": {"achieved": alg_bytes / kernel_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": alg_bytes / kernel_s / 1e9 / peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} HBM copy bandwidth"},
+    }
+    intensity = flops / alg_bytes
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    bound = "hbm" if intensity < ridge else "tensor"
+    r = roofs[bound]
+    roofline = {"bound": bound, "achieved": r["achieved"], "peak": r["peak"], "unit": r["unit"],
+                "frac": r["frac"], "traffic": None, "peak_source": r["peak_source"],
+                "algorithmic_bytes": alg_bytes, "algorithmic_flop": flops,
+                "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
+    return roofline, roofs
+
+
+def config_dict(w, ws):
+    """The workload description both arms print (identical for the same run)."""
+    kv = w.cu_seqlens_k is not None
+    return {"workload": w.name,
+            "seqlens": w.seqlens if len(w.seqlens) <= 8 else f"{len(w.seqlens)} seqs",
+            "total_tokens": w.total_tokens,
+            "key_lengths": (w.seqlens_k if kv and len(w.seqlens_k) <= 8 else
+                            (f"{len(w.seqlens_k)} seqs, {w.total_keys} keys" if kv else None)),
+            "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "window": w.window, "scale": w.scale,
+            "sinks": w.sinks is not None, "lse": True,
+            "inputs": "fp8 e4m3 (per-tensor scales)" if w.fp8 is not None else "bf16",
+            "l2": "flushed before every timed GPU step (256 MB write, then 256 MB read)",
+            "parallelism": "replicas" if ws > 1 else "single GPU"}
+
+
+def parity_stats(gpu_out, gpu_lse, ref_out, ref_lse):
+    """max/mean |d| of sampled output rows ([n, D]) and max |d| of their LSE ([n])."""
+    o = gpu_out.astype(np.float64)
+    d = np.abs(o - ref_out)
+    dl = np.abs(gpu_lse.astype(np.float64) - ref_lse)
+    return {"rows": int(len(o)), "out_max_abs": float(d.max()), "out_mean_abs": float(d.mean()),
+            "lse_max_abs": float(dl.max()), "finite": bool(np.isfinite(o).all())}
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
@@ -215,26 +268,27 @@ def run_reference(args, ws, rank):
     # each step: the oracle on a bounded row sample (~3 s of CPU work)
     for _ in range(args.warmup):
         oracle_rate(w, 0.5)
-    rates, secs, rows, thr = [], [], 0, 0
+    rates, step_s, rows, thr = [], [], 0, 0
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         r, n, dt, thr, fl = oracle_rate(w, 3.0)
+        step_s.append(time.perf_counter() - t0)
         rates.append(r)
-        secs.append(dt)
         rows = n
     value = statistics.median(rates) / 1e12
-    ms_equiv = flops_total / (value * 1e12) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_equiv, "higher_is_better": True, "scaling": "weak",
+        # measured wall time of one step (a bounded row sample, rate calibration included)
+        "ms_per_step": statistics.mean(step_s) * 1e3,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
-                   f"{len(w.seqlens)} seqs", "key_lengths": w.seqlens_k,
-                   "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "window": w.window, "note": "ms_per_step extrapolated from the sampled rate"},
+        "config": config_dict(w, ws),
+        "step": f"the CPU oracle on {rows} uniform (token, head) rows of the workload",
+        "ms_per_full_workload_extrapolated": flops_total / (value * 1e12) * 1e3,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                          "sample": f"{rows} uniform (token, head) rows per step of {w.name}, "
-                                   f"~{statistics.median(secs):.1f} s each"},
+                                   f"~{statistics.mean(step_s):.1f} s each"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -416,49 +470,41 @@ def main():
         return 0
 
     peaks, peak_src = load_peaks()
-    if decode:
-        # A stream over the cache (about 4 FLOP per byte): the HBM roof applies.
-        achieved = w.algorithmic_bytes() / (attn_avg * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name, D, True),
-                    "peak_source": f"{peak_src} HBM copy bandwidth",
-                    "algorithmic_bytes": w.algorithmic_bytes(),
-                    "kernel": f"decode_split_kernel<{D}> (merging its splits)"}
-    else:
-        achieved = flops / (attn_avg * 1e-3) / 1e12
-        # E4M3 contractions: twice the dense bf16 rate (the nominal fp8/bf16 ratio)
-        peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
-        roofline = {"bound": "tensor", "achieved": achieved,
-                    "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": ncu_traffic(w.name, D, False, fp8),
-                    "peak_source": (f"{peak_src} dense bf16 (burst) x 2 for E4M3" if fp8 else
-                                    f"{peak_src} dense bf16 (burst)"),
-                    "algorithmic_bytes": w.algorithmic_bytes(),
-                    "kernel": ("attention_fwd_fp8_kernel" if fp8 else
-                               "attention_fwd_d128_kernel" if D == 128 else
-                               "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
-                               "attention_fwd_kernel<false>")}
+    kernel_s = attn_avg * 1e-3
+    alg_bytes = w.algorithmic_bytes()
+    kernel_name = ("decode_split_kernel<%d> (merging its splits)" % D if decode else
+                   "attention_fwd_fp8_kernel" if fp8 else
+                   "attention_fwd_d128_kernel" if D == 128 else
+                   "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
+                   "attention_fwd_kernel<false>")
+    traffic = ncu_traffic(w.name, D, decode, fp8)
+    roofline, roofs = roofline_of(flops, alg_bytes, kernel_s, peaks, peak_src, fp8)
+    roofline.update(traffic=traffic, kernel=kernel_name)
+    # Exponentials: one per allowed (query, key, head) triple, i.e. the
+    # unmasked FLOP over 4 D, against the measured rate of the exponential
+    # instruction the softmax uses.
+    ex2_peak = pkg.tsk_bench_ex2_rate(stream)
+    exps = flops / (4.0 * D)
+    exp_roof = {"achieved": exps / kernel_s / 1e9, "peak": ex2_peak / 1e9, "unit": "Gexp/s",
+                "frac": exps / kernel_s / ex2_peak,
+                "peak_source": "measured ex2.approx.f32 throughput (tsk_bench_ex2_rate, this run)",
+                "note": "algorithmic exponentials (unmasked scores); the kernel also evaluates "
+                        "masked positions of tiles that straddle the diagonal or window edge"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (fp32 accumulation)" if fp8 else "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, fp32 sinks)",
-        "config": {"workload": w.name, "seqlens": w.seqlens if len(w.seqlens) <= 8 else
-                   f"{len(w.seqlens)} seqs", "total_tokens": T,
-                   "key_lengths": (w.seqlens_k if kvcache and len(w.seqlens_k) <= 8 else
-                                   (f"{len(w.seqlens_k)} seqs, {w.total_keys} keys" if kvcache
-                                    else None)),
-                   "Hq": Hq, "Hkv": Hkv, "D": D,
-                   "window": w.window, "scale": w.scale, "sinks": True, "lse": True,
-                   "l2": "flushed before every timed step (256 MB write, then 256 MB read)",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "data": "synthetic (seeded N(0,1) Q/K/V, fp32 sinks)",
+        "config": config_dict(w, ws),
         "tokens_per_s": T * ws / (ms * 1e-3),
         "pct_of_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
         "unmasked_flop_per_step": flops,
         "attention_kernel_ms": attn_avg, "prepass_kernel_ms": sum(pre_ms) / len(pre_ms),
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
         "roofline": roofline,
+        "roofs": roofs,
+        "exp": exp_roof,
         "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "matches_resident_run": bool(same),
@@ -472,11 +518,25 @@ def main():
         "kernel_source_hash": kernel_source_hash(D, decode, fp8),
     }
     if not args.no_cpu_baseline:
-        r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds)
+        # The CPU oracle on a bounded uniform sample of (token, head) rows: its
+        # rate is the baseline, and its values for those rows check the output
+        # of the last timed step.
+        keep = {}
+        r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds, keep=keep)
         line["cpu_baseline"] = {"value": r / 1e12, "unit": "TFLOP/s", "cores": thr,
                                 "kind": "oracle",
                                 "sample": f"{n} uniform (token, head) rows of {w.name} "
                                           f"({fl / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+        ti = torch.from_numpy(keep["t"]).to(dev)
+        hi = torch.from_numpy(keep["h"].astype(np.int64)).to(dev)
+        g_out = out[ti, hi].float().cpu().numpy()
+        g_lse = lse[ti, hi].cpu().numpy()
+        line["parity"] = dict(
+            parity_stats(g_out, g_lse, keep["out"], keep["lse"]),
+            of="the timed run's output (last step) at the cpu_baseline's sampled rows, "
+               "against the CPU oracle",
+            tolerance={"out_max_abs": 2e-2, "out_mean_abs": 2e-3, "lse_max_abs": 1e-3}
+            if not fp8 else "E4M3 rounding bound (see tests/test_parity_fp8_gpu.py)")
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

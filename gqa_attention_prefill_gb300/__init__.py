@@ -21,9 +21,10 @@ import threading
 
 __all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "tsk_mha_prefill_kvcache",
            "tsk_mha_decode_kvcache", "tsk_mha_prefill_paged", "tsk_mha_decode_paged", "tsk_mha_prefill_fp8", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
-           "tsk_get_device_status", "tsk_status_string",
+           "tsk_get_device_status", "tsk_noalloc_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
+           "tsk_bench_ex2_rate",
            "tsk_version", "TskError", "library_path", "load_library"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -99,11 +100,15 @@ def load_library():
         lib.tsk_last_error.restype = ctypes.c_char_p
         lib.tsk_get_device_status.argtypes = [P]
         lib.tsk_get_device_status.restype = ctypes.c_int
+        lib.tsk_noalloc_status.argtypes = [P]
+        lib.tsk_noalloc_status.restype = ctypes.c_int
         lib.tsk_profile_enable.argtypes = [ctypes.c_int]
         lib.tsk_profile_enable.restype = ctypes.c_int
         lib.tsk_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_float)]
         lib.tsk_profile_read.restype = ctypes.c_int
+        lib.tsk_bench_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), P]
+        lib.tsk_bench_ex2_rate.restype = ctypes.c_int
         lib.tsk_kernels_per_call.argtypes = []
         lib.tsk_kernels_per_call.restype = i32
         lib.tsk_release.argtypes = []
@@ -344,6 +349,11 @@ def tsk_get_device_status(stream=None) -> int:
     return load_library().tsk_get_device_status(_stream_handle(stream))
 
 
+def tsk_noalloc_status(stream=None) -> int:
+    """Device-side status of the most recent tsk_mha_prefill_noalloc call."""
+    return load_library().tsk_noalloc_status(_stream_handle(stream))
+
+
 def tsk_profile_enable(enable: bool = True) -> int:
     return load_library().tsk_profile_enable(1 if enable else 0)
 
@@ -360,6 +370,15 @@ def tsk_profile_read():
 def tsk_debug_set_wait(timeout_ns: int = 0, stall: bool = False) -> int:
     """Test hook: device wait limit for later calls (0 = 2 s) and stall injection."""
     return load_library().tsk_debug_set_wait(int(timeout_ns), 1 if stall else 0)
+
+
+def tsk_bench_ex2_rate(stream=None) -> float:
+    """Measured exponential (ex2.approx.f32) throughput of the device, per second."""
+    r = ctypes.c_double()
+    rc = load_library().tsk_bench_ex2_rate(ctypes.byref(r), _stream_handle(stream))
+    if rc != 0:
+        raise TskError(rc, "tsk_bench_ex2_rate")
+    return r.value
 
 
 def tsk_kernels_per_call() -> int:

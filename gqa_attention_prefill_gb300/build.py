@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libtsk_mha.so")
 SOURCES = [os.path.join(CSRC, "tsk_mha.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attention.cuh", "attention_d128.cuh", "attention_fp8.cuh", "decode.cuh", "ptx.cuh", "schedule.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attention.cuh", "attention_d128.cuh", "attention_fp8.cuh", "decode.cuh", "ptx.cuh", "schedule.cuh", "probe.cuh")] + [
     os.path.join(ROOT, "include", "tsk_mha.h")]
 
 

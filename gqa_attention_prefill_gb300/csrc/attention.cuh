@@ -212,6 +212,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   // ------------------------------------------------------------ producer
   uint32_t q_iter = 0, kv_iter = 0;
   bool ok = true;
+  TSK_TL_DECL;
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit<QS>(p, u);
@@ -228,6 +229,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
       const uint32_t k = kv_iter / kStages;
       if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, 2, p, cx.abort);
       if (!ok) break;
+      TSK_EV(30);
       const int pos0 = (w.kv_lo + j) * kTileN;  // key position of the tile's first key
       const int Lk = w.offset + w.len;
       const uint32_t kdst = cx.sbase + kSmemKV + s * 2 * kTileBytes;
@@ -262,6 +264,7 @@ template <int QS>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
   bool ok = true;
+  TSK_TL_DECL;
   const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
   const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
   const uint32_t a_p = cx.tmem + kColP0 + 64 * t;
@@ -278,6 +281,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
     if (!ok) break;
     const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes;
     auto issue_s = [&](int stage) {
+      TSK_EV(21);
       TSK_TRACE_T0(tr_is);
       const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes;
 #pragma unroll
@@ -286,6 +290,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
                kk > 0 ? 1u : 0u);
       tc_commit(cx.bar(kBarSFull + t));
       ++s_cnt;
+      TSK_EV(22);
       TSK_TRACE_ADD(15, tr_is);
     };
     {  // S_t(0)
@@ -301,15 +306,18 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       const int sc = cur % kStages;
       if (j + 1 < w.n_kv) {
         const int sn = (cur + 1) % kStages;
+        TSK_EV(20);
         ok = mbar_wait(cx.bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, 6, p, cx.abort);
         if (ok) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5, p, cx.abort);
         if (!ok) break;
         tc_fence_after();
         issue_s(sn);
       }
+      TSK_EV(23);
       ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStages) & 1, 7, p, cx.abort);
       if (ok) ok = mbar_wait(cx.bar(kBarPFull + t), p_cnt & 1, 8, p, cx.abort);
       if (!ok) break;
+      TSK_EV(24);
       tc_fence_after();
       const uint32_t b = cx.sbase + kSmemKV + sc * 2 * kTileBytes + kTileBytes;
       TSK_TRACE_T0(tr_ip);
@@ -319,6 +327,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
                (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(cx.bar(kBarPVDone + t));
       ++p_cnt;
+      TSK_EV(25);
       TSK_TRACE_ADD(16, tr_ip);
       for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarKVEmpty + sc));
     }
@@ -376,9 +385,11 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
   uint32_t s_cnt = 0, pv_cnt = 0;
+  TSK_TL_DECL;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    TSK_EV(8);
     TSK_TRACE_T0(tr_dec);
     // Only what the key loop needs is kept from the unit; the epilogue reads
     // the sequence fields again (registers are the scarce resource here).
@@ -399,8 +410,10 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     TSK_TRACE_ADD(24, tr_dec);
     for (int j = 0; j < n_kv; ++j) {
       const int kt = kv_lo + j;
+      TSK_EV(1);
       ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort);
       if (!ok) break;
+      TSK_EV(2);
       ++s_cnt;
       tc_fence_after();
       TSK_TRACE_T0(tr_ld);
@@ -412,6 +425,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       tmem_wait_ld();
       reg_fence<128>(sr);
       TSK_TRACE_ADD(20, tr_ld);
+      TSK_EV(3);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
@@ -453,6 +467,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       }
       const float m_tile = max3f(m0, m1, fmaxf(m2, m3)) * sl2;
       TSK_TRACE_ADD(21, tr_max);
+      TSK_EV(4);
       float alpha = 1.f;
       const bool need = m_tile > m_used + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
@@ -481,10 +496,12 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       }
       l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       TSK_TRACE_ADD(22, tr_exp);
+      TSK_EV(5);
       if (j > 0) {
         // O_t is stable and P_t reusable once PV_t(j-1) has completed.
         ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
         if (!ok) break;
+        TSK_EV(6);
         ++pv_cnt;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -507,9 +524,11 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
+      TSK_EV(7);
     }
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
+    TSK_EV(9);
     const int per_tile = p.Hkv * p.HP;
     const int qi = u / per_tile;
     int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
@@ -524,6 +543,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
     TSK_TRACE_T0(tr_epi);
     if (!ok) break;
+    TSK_EV(10);
     ++pv_cnt;
     tc_fence_after();
     uint32_t o[64];
@@ -563,6 +583,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     }
     tc_fence_before();
     TSK_TRACE_ADD(28, tr_epi);
+    TSK_EV(11);
   }
   if (lane == 0) bulk_wait_group0();  // every output store of this warp has completed
   TSK_TRACE_ADD(30, tr_all);

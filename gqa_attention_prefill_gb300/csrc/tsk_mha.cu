@@ -20,6 +20,7 @@
 #include "decode.cuh"
 #include "attention_fp8.cuh"
 #include "schedule.cuh"
+#include "probe.cuh"
 
 namespace {
 
@@ -283,6 +284,34 @@ tsk_status tsk_debug_timeline(unsigned long long* out, int32_t n) {
 }
 
 int32_t tsk_kernels_per_call(void) { return 2; }
+
+// Exponential-unit throughput of the current device (one warm-up launch,
+// then one launch timed with CUDA events on `stream`).
+tsk_status tsk_bench_ex2_rate(double* ex2_per_second, tsk_stream_t stream_) {
+  if (!ex2_per_second) return TSK_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = -1, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cuda_fail(cudaErrorNoDevice);
+  constexpr int kIters = 1 << 14;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+    return cuda_fail(cudaErrorUnknown, "tsk_bench_ex2_rate: events");
+  tsk::ex2_rate_kernel<<<sms, tsk::kEx2ProbeThreads, 0, stream>>>(kIters / 8);
+  cudaEventRecord(e0, stream);
+  tsk::ex2_rate_kernel<<<sms, tsk::kEx2ProbeThreads, 0, stream>>>(kIters);
+  cudaEventRecord(e1, stream);
+  cudaError_t e = cudaEventSynchronize(e1);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess || !(ms > 0.f)) return cuda_fail(e, "tsk_bench_ex2_rate");
+  *ex2_per_second = (double)sms * tsk::kEx2ProbeThreads * tsk::kEx2ProbeChains * kIters /
+                    (ms * 1e-3);
+  return TSK_OK;
+}
 
 }  // extern "C"
 
@@ -679,6 +708,32 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
     return TSK_ERR_LAUNCH;
   }
   return TSK_OK;
+}
+
+// Status words of the allocation-free call: the array holds those of the
+// most recent call on the current device (each call clears them first).
+extern "C" tsk_status tsk_noalloc_status(tsk_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TSK_ERR_DEVICE;
+    auto it = g_noalloc_ptr.find(dev);
+    if (it == g_noalloc_ptr.end() || !it->second) return TSK_OK;  // no call on this device yet
+    scratch = it->second;
+  }
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tsk_noalloc_status: stream synchronise");
+  int hdr[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(hdr, scratch + tsk::kWsStatus, sizeof hdr, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "tsk_noalloc_status: read");
+  if (hdr[0] != 0) {
+    const int zero[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(scratch + tsk::kWsStatus, zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "tsk_noalloc_status: clear");
+  }
+  return (tsk_status)hdr[0];
 }
 
 // ---------------------------------------------------------------------------

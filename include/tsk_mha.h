@@ -237,6 +237,16 @@ TSK_API tsk_status tsk_profile_read(float *prepass_ms, float *attention_ms);
 /* Number of kernels one tsk_mha_prefill call launches (0 for empty problems). */
 TSK_API int32_t tsk_kernels_per_call(void);
 
+/*
+ * Benchmark helper (not part of the attention path): measures the current
+ * device's throughput of the exponential instruction the softmax uses
+ * (ex2.approx.f32), with 16 warps per SM running independent chains, and
+ * stores it in *ex2_per_second (exponentials per second over the whole GPU).
+ * Synchronises `stream`.  The benchmark states the softmax's exponentials
+ * per second against this roof.
+ */
+TSK_API tsk_status tsk_bench_ex2_rate(double *ex2_per_second, tsk_stream_t stream);
+
 /* Frees every cached workspace (synchronises the device first). */
 TSK_API tsk_status tsk_release(void);
 
@@ -293,14 +303,28 @@ TSK_API tsk_status tsk_debug_timeline(unsigned long long *out, int32_t n);
  * work overlaps on the GPU (different streams, or host threads issuing
  * concurrently) race and must be serialised by the caller.  Each call clears
  * the status words it needs; device-side errors it detects (inconsistent
- * cu_seqlens, an expired bounded wait) leave the outputs unwritten but are
- * not reported by tsk_get_device_status.
+ * cu_seqlens, an expired bounded wait) leave the outputs unwritten and are
+ * reported by tsk_noalloc_status (below), not by tsk_get_device_status.
  */
 TSK_API tsk_status tsk_mha_prefill_noalloc(const void *q, const void *k, const void *v,
                                            const float *sinks, const int32_t *cu_seqlens,
                                            int32_t num_seqs, int64_t total_tokens, int32_t Hq,
                                            int32_t Hkv, int32_t D, int32_t window, float scale,
                                            void *out, float *lse, tsk_stream_t stream);
+
+/*
+ * tsk_noalloc_status -- the device-side status of the most recent
+ * tsk_mha_prefill_noalloc call on the current device: TSK_OK, or
+ * TSK_ERR_BAD_SEQLENS (-8, cu_seqlens inconsistent with num_seqs or
+ * total_tokens; nothing was written) or TSK_ERR_DEVICE_TIMEOUT (-7, a bounded
+ * wait expired).  Like tsk_get_device_status it synchronises `stream` (the
+ * stream that call was made on) and clears a non-zero status after reading
+ * it; it allocates nothing (two small synchronous copies of the fixed
+ * array's status words).  Returns TSK_OK if no allocation-free call has been
+ * made on this device.  (No counterpart in the pages: a companion of the
+ * allocation-free entry point.)
+ */
+TSK_API tsk_status tsk_noalloc_status(tsk_stream_t stream);
 
 /*
  * tsk_mha_prefill_host -- tsk_mha_prefill with every buffer in host memory:

@@ -44,3 +44,55 @@ def test_committed_traffic_entries_are_well_formed():
     for name, e in d.items():
         assert e["dram_bytes_per_launch"] > 0 and len(e["kernel_source_hash"]) == 16, name
         assert "kernel" in e and "source" in e, name
+
+
+PEAKS = {"bf16_tflops": 1930.3, "bf16_tflops_sustained": 1729.1, "hbm_gbs": 6792.4}
+
+
+def test_binding_roof_follows_the_arithmetic_intensity():
+    import inputgen
+    b = _bench()
+    c1 = inputgen.config("causal_4x4096_h64kv8")
+    c2 = inputgen.config("window128_4x4096_h64kv8")
+    r1, roofs1 = b.roofline_of(c1.unmasked_flops(), c1.algorithmic_bytes(), 6e-4, PEAKS, "m")
+    r2, roofs2 = b.roofline_of(c2.unmasked_flops(), c2.algorithmic_bytes(), 1.5e-4, PEAKS, "m")
+    assert r1["bound"] == "tensor" and r1["unit"] == "TFLOP/s"
+    assert r2["bound"] == "hbm" and r2["unit"] == "GB/s"
+    # both roofs are always reported; the line's roofline is the binding one
+    assert r2["frac"] == roofs2["hbm"]["frac"] and r1["frac"] == roofs1["tensor"]["frac"]
+    assert abs(roofs2["hbm"]["achieved"] - c2.algorithmic_bytes() / 1.5e-4 / 1e9) < 1e-6
+    # E4M3 doubles the tensor roof, which moves the ridge point
+    r3, _ = b.roofline_of(c1.unmasked_flops(), c1.algorithmic_bytes(), 6e-4, PEAKS, "m", True)
+    assert r3["peak"] == 2 * PEAKS["bf16_tflops"]
+
+
+def test_parity_stats():
+    import numpy as np
+    b = _bench()
+    ref = np.zeros((3, 4))
+    out = ref.copy()
+    out[1, 2] = 0.5
+    st = b.parity_stats(out, np.array([0.0, 1e-4, 0.0]), ref, np.zeros(3))
+    assert st["rows"] == 3 and st["out_max_abs"] == 0.5 and st["finite"]
+    assert abs(st["out_mean_abs"] - 0.5 / 12) < 1e-15 and abs(st["lse_max_abs"] - 1e-4) < 1e-15
+
+
+def test_reference_arm_reports_its_measured_step_time_and_the_same_config():
+    import subprocess
+    import sys
+    import time
+    import inputgen
+    b = _bench()
+    t0 = time.perf_counter()
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_1x256_h4kv1", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300)
+    wall = time.perf_counter() - t0
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == json.loads(json.dumps(
+        b.config_dict(inputgen.config("tiny_1x256_h4kv1"), 1)))
+    # a measured time (at most the process's wall time), not an extrapolation
+    assert 0 < line["ms_per_step"] <= wall * 1e3
+    assert line["ms_per_full_workload_extrapolated"] > 0

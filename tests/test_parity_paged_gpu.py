@@ -127,3 +127,14 @@ def test_bad_page_index_reported(decode):
     out, lse, st = run_paged(w, 64, decode=decode, table_edit=corrupt, check_status=False)
     assert st == -8
     assert torch.isnan(out.float()).all()
+
+
+@pytest.mark.parametrize("page_size", [16, 128])
+@pytest.mark.parametrize("window", [0, 200])
+def test_prefill_one_query_head_per_kv_head(page_size, window):
+    # Hq == Hkv: a work unit is two consecutive 128-row tiles of one head, the
+    # second tile's keys read through the block table too; an odd number of
+    # query tiles in the second sequence, sequence ends inside either tile
+    w = inputgen.make_kvcache([129, 300], [700, 2500], 4, 4, window=window,
+                              seed=page_size + window)
+    print(check(w, page_size, label=f"prefill G=1 page={page_size} W={window}"))
