@@ -38,13 +38,15 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, out: str | None = None,
-          defines=()) -> str:
-    """Builds libtsk_mha.so (or `out`, with extra -D `defines`, always rebuilt)."""
+          defines=(), host_flags=()) -> str:
+    """Builds libtsk_mha.so (or `out`, with extra -D `defines` and host-compiler
+    flags, always rebuilt)."""
     target = out or LIB
-    if out is None and not defines and not force and not stale():
+    if out is None and not defines and not host_flags and not force and not stale():
         return LIB
     tmp = target + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *flags(verbose), *[f"-D{d}" for d in defines], "-o", tmp, *SOURCES]
+    hf = [x for f in host_flags for x in ("-Xcompiler", f)]
+    cmd = [nvcc(), *flags(verbose), *[f"-D{d}" for d in defines], *hf, "-o", tmp, *SOURCES]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

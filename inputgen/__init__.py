@@ -32,21 +32,23 @@ _lib = None
 STREAM_Q, STREAM_K, STREAM_V, STREAM_SINKS, STREAM_LENS, STREAM_ROWS = 1, 2, 3, 4, 5, 6
 
 
-def build_lib(force: bool = False) -> str:
-    """Compile gen.c into libinputgen.so next to it (plain gcc, portable C)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC,
-                               "-lm", "-lpthread"])
-        os.replace(tmp, _LIB)
-    return _LIB
+def build_lib(force: bool = False, extra_flags=(), out_path: str | None = None) -> str:
+    """Compile gen.c into libinputgen.so next to it (plain gcc, portable C), or
+    into `out_path` with extra compiler flags."""
+    out = out_path or _LIB
+    if force or out_path or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", *extra_flags, "-o",
+                               tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, out)
+    return out
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build_lib())
+            lib = ctypes.CDLL(os.environ.get("INPUTGEN_LIB_PATH") or build_lib())
             lib.ig_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
                                            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
             lib.ig_normal_bf16.restype = None

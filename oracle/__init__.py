@@ -67,10 +67,12 @@ def _bind(lib):
 
 
 def _load():
+    """The oracle library: $ORACLE_LIB_PATH if set (another build of the same
+    source, e.g. with sanitizers), else the in-tree build."""
     global _lib
     with _lock:
         if _lib is None:
-            _lib = _bind(ctypes.CDLL(build_lib()))
+            _lib = _bind(ctypes.CDLL(os.environ.get("ORACLE_LIB_PATH") or build_lib()))
     return _lib
 
 
