@@ -35,6 +35,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "schedule.cuh"
@@ -49,6 +50,14 @@ namespace tsk {
 #endif
 constexpr int kStages = TSK_KV_STAGES;           // K/V ring depth
 constexpr float kRescaleThreshold = TSK_RESCALE_THRESHOLD;  // log2 units
+// A key tile of the causal kernel skips its row maximum when the bound on its
+// scores lies within this much (log2 units) of the maximum in use: then every
+// p <= 2^64.  With l kept below 2^32 between tiles (see the fast tile), a tile
+// adds at most 128 * 2^64 to l, so |O| <= l max|v| stays finite for
+// |v| < 2^56.
+constexpr float kFastLag = 64.f;
+struct SlowTile : std::true_type {};
+struct FastTile : std::false_type {};
 constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kSoftmaxWarpsPerTile = 4;
 constexpr int kThreads = 32 * (kFirstSoftmaxWarp + 2 * kSoftmaxWarpsPerTile);
@@ -58,9 +67,10 @@ constexpr uint32_t kSmemQ = 0;                           // 2 buffers x 2 tiles
 constexpr uint32_t kSmemKV = 4 * kTileBytes;             // kStages x (K, V)
 constexpr uint32_t kSmemBar = kSmemKV + kStages * 2 * kTileBytes;  // barriers (< 512 B)
 constexpr uint32_t kSmemEpi = kSmemBar + 1024;  // 2 output staging tiles
+constexpr uint32_t kSmemNorm = kSmemEpi + 2 * kTileBytes;  // key-norm bound per KV head
 // Dynamic shared memory per kernel variant, + 1 KB slack for the alignment.
-constexpr uint32_t kSmemBytesCausal = kSmemEpi + 2 * kTileBytes + 1024;
-constexpr uint32_t kSmemBytesWindow = kSmemEpi + 2 * kTileBytes + 1024;
+constexpr uint32_t kSmemBytesCausal = kSmemNorm + 4 * kNormMaxHeads + 1024;
+constexpr uint32_t kSmemBytesWindow = kSmemNorm + 4 * kNormMaxHeads + 1024;
 
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
 constexpr uint32_t kTmemCols = 512;
@@ -81,6 +91,7 @@ struct AttnParams {
   unsigned long long timeout_ns;
   int debug_stall;      // test hook: producer first waits on a barrier nothing signals
   PagedKV kv;           // paged key/value cache, or kv.page_size == 0 (contiguous)
+  const float* knorm = nullptr;  // [Hkv] largest key-row norm per KV head, or nullptr
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.
@@ -201,6 +212,10 @@ struct Ctx {
   int total_units;
   uint32_t abort;   // shared address of the CTA's abort flag
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+  // Largest key-row norm of KV head g (copied to shared memory at the start).
+  __device__ __forceinline__ float knorm_smem(int g) const {
+    return ld_shared_f32(sbase + kSmemNorm + 4u * (uint32_t)g);
+  }
 };
 
 
@@ -264,6 +279,10 @@ template <int QS>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
   bool ok = true;
+#define TSK_ISSUER_WAIT(bar, par, site) mbar_wait(bar, par, site, p, cx.abort)
+#define TSK_MMA_SS(...) mma_ss(__VA_ARGS__)
+#define TSK_MMA_TS(...) mma_ts(__VA_ARGS__)
+#define TSK_COMMIT(bar) tc_commit(bar)
   TSK_TL_DECL;
   const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
   const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
@@ -277,7 +296,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       continue;
     }
     const int commits = w.ntiles == 1 ? 2 : 1;  // arrivals owed on the shared release barriers
-    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3, p, cx.abort);
+    ok = TSK_ISSUER_WAIT(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3);
     if (!ok) break;
     const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes;
     auto issue_s = [&](int stage) {
@@ -286,17 +305,17 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        mma_ss(d_s, sdesc_sw128(qaddr + 32 * kk), sdesc_sw128(b + 32 * kk), kIdescQK,
+        TSK_MMA_SS(d_s, sdesc_sw128(qaddr + 32 * kk), sdesc_sw128(b + 32 * kk), kIdescQK,
                kk > 0 ? 1u : 0u);
-      tc_commit(cx.bar(kBarSFull + t));
+      TSK_COMMIT(cx.bar(kBarSFull + t));
       ++s_cnt;
       TSK_EV(22);
       TSK_TRACE_ADD(15, tr_is);
     };
     {  // S_t(0)
       const int s0 = kv_iter % kStages;
-      ok = mbar_wait(cx.bar(kBarKFull + s0), (kv_iter / kStages) & 1, 4, p, cx.abort);
-      if (ok && s_cnt > 0) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5, p, cx.abort);
+      ok = TSK_ISSUER_WAIT(cx.bar(kBarKFull + s0), (kv_iter / kStages) & 1, 4);
+      if (ok && s_cnt > 0) ok = TSK_ISSUER_WAIT(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5);
       if (!ok) break;
       tc_fence_after();
       issue_s(s0);
@@ -307,15 +326,15 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       if (j + 1 < w.n_kv) {
         const int sn = (cur + 1) % kStages;
         TSK_EV(20);
-        ok = mbar_wait(cx.bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, 6, p, cx.abort);
-        if (ok) ok = mbar_wait(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5, p, cx.abort);
+        ok = TSK_ISSUER_WAIT(cx.bar(kBarKFull + sn), ((cur + 1) / kStages) & 1, 6);
+        if (ok) ok = TSK_ISSUER_WAIT(cx.bar(kBarSFree + t), (s_cnt - 1) & 1, 5);
         if (!ok) break;
         tc_fence_after();
         issue_s(sn);
       }
       TSK_EV(23);
-      ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStages) & 1, 7, p, cx.abort);
-      if (ok) ok = mbar_wait(cx.bar(kBarPFull + t), p_cnt & 1, 8, p, cx.abort);
+      ok = TSK_ISSUER_WAIT(cx.bar(kBarVFull + sc), (cur / kStages) & 1, 7);
+      if (ok) ok = TSK_ISSUER_WAIT(cx.bar(kBarPFull + t), p_cnt & 1, 8);
       if (!ok) break;
       TSK_EV(24);
       tc_fence_after();
@@ -323,22 +342,26 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       TSK_TRACE_T0(tr_ip);
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk)
-        mma_ts(d_o, a_p + 8 * kk, sdesc_sw128(b + 2048 * kk), kIdescPV,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(cx.bar(kBarPVDone + t));
+        TSK_MMA_TS(d_o, a_p + 8 * kk, sdesc_sw128(b + 2048 * kk), kIdescPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+      TSK_COMMIT(cx.bar(kBarPVDone + t));
       ++p_cnt;
       TSK_EV(25);
       TSK_TRACE_ADD(16, tr_ip);
-      for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarKVEmpty + sc));
+      for (int c = 0; c < commits; ++c) TSK_COMMIT(cx.bar(kBarKVEmpty + sc));
     }
     if (!ok) break;
     kv_iter += w.n_kv;
-    for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarQEmpty + qb));
+    for (int c = 0; c < commits; ++c) TSK_COMMIT(cx.bar(kBarQEmpty + qb));
     ++q_iter;
   }
   // Make sure none of this thread's MMAs is still running before TMEM is freed.
-  tc_commit(cx.bar(kBarDrain + t));
+  TSK_COMMIT(cx.bar(kBarDrain + t));
   mbar_wait<true>(cx.bar(kBarDrain + t), 0, 14, p, cx.abort);
+#undef TSK_ISSUER_WAIT
+#undef TSK_MMA_SS
+#undef TSK_MMA_TS
+#undef TSK_COMMIT
 }
 
 // Column chunks of a 128-key tile (32 keys each) classified for one warp:
@@ -384,7 +407,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
   const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
-  uint32_t s_cnt = 0, pv_cnt = 0;
+  uint32_t s_cnt = 0, pv_cnt = 0, q_iter = 0;
   TSK_TL_DECL;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
@@ -393,11 +416,15 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     TSK_TRACE_T0(tr_dec);
     // Only what the key loop needs is kept from the unit; the epilogue reads
     // the sequence fields again (registers are the scarce resource here).
-    int n_kv, kv_lo, diag0, pos;
+    int n_kv, kv_lo, diag0, pos, gk;
     float m_used = -INFINITY, l = 0.f;
+    const int qb = q_iter & 1;
+    const uint32_t q_par = (q_iter >> 1) & 1;
+    ++q_iter;
     {
       const Unit w = decode_unit<QS>(p, u);
       if (t >= w.ntiles) continue;
+      gk = w.g;
       n_kv = w.n_kv;
       kv_lo = w.kv_lo;
       diag0 = w.offset + tile_q0<QS>(w, t);  // key position of the tile's first query row
@@ -408,11 +435,44 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       }
     }
     TSK_TRACE_ADD(24, tr_dec);
-    for (int j = 0; j < n_kv; ++j) {
+    // Bound on x = s * scale * log2(e) for every key of this row: ||q|| times
+    // the largest key norm of the KV head (Cauchy-Schwarz).
+    float bq = INFINITY;
+    if (p.knorm) {
+      TSK_EV(16);
+      ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
+      if (!ok) break;
+      TSK_EV(18);
+      // the row's 128 bytes (8 chunks of 16, permuted by the swizzle)
+      const uint32_t qrow = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes + (uint32_t)r * 128u;
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        // chunk k ^ (r & 7): the lanes of a warp spread over all 32 banks
+        const uint4 v = ld_shared_v4(qrow + 16u * (uint32_t)(k ^ (r & 7)));
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
+      }
+      bq = sl2 * sqrtf(ss) * cx.knorm_smem(gk);
+      TSK_EV(19);
+    }
+    // One key tile.  A slow tile computes its row maximum and raises the
+    // maximum in use, m_used, when the tile exceeds it by more than
+    // kRescaleThreshold (p <= 2^8 then).  A fast tile skips the maximum and
+    // keeps m_used, which the bound allows while bq - m_used <= kFastLag for
+    // every row of the warp (p <= 2^40).  m_used only changes in slow tiles,
+    // so once a tile is fast the rest of the unit is.
+    auto step = [&](int j, auto slow_tag) -> bool {
+      constexpr bool kSlow = decltype(slow_tag)::value;
       const int kt = kv_lo + j;
       TSK_EV(1);
-      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort);
-      if (!ok) break;
+      if (!mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort))
+        return false;
       TSK_EV(2);
       ++s_cnt;
       tc_fence_after();
@@ -455,28 +515,40 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
         }
       }
       TSK_TRACE_ADD(27, tr_mask);
-      // Row maximum: four independent chains of 3-input max.
-      TSK_TRACE_T0(tr_max);
-      float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
-#pragma unroll
-      for (int c = 4; c < 128; c += 8) {
-        m0 = max3f(m0, s[c + 0], s[c + 1]);
-        m1 = max3f(m1, s[c + 2], s[c + 3]);
-        m2 = max3f(m2, s[c + 4], s[c + 5]);
-        m3 = max3f(m3, s[c + 6], s[c + 7]);
-      }
-      const float m_tile = max3f(m0, m1, fmaxf(m2, m3)) * sl2;
-      TSK_TRACE_ADD(21, tr_max);
-      TSK_EV(4);
       float alpha = 1.f;
-      const bool need = m_tile > m_used + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        if (m_tile > m_used) {
-          alpha = ex2_approx(m_used - m_tile);  // m_used = -inf gives 0
-          m_used = m_tile;
+      if constexpr (kSlow) {
+        // Row maximum: four independent chains of 3-input max.
+        TSK_TRACE_T0(tr_max);
+        float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 8) {
+          m0 = max3f(m0, s[c + 0], s[c + 1]);
+          m1 = max3f(m1, s[c + 2], s[c + 3]);
+          m2 = max3f(m2, s[c + 4], s[c + 5]);
+          m3 = max3f(m3, s[c + 6], s[c + 7]);
+        }
+        const float m_tile = max3f(m0, m1, fmaxf(m2, m3)) * sl2;
+        TSK_TRACE_ADD(21, tr_max);
+        if (__any_sync(0xffffffffu, m_tile > m_used + kRescaleThreshold)) {
+          if (m_tile > m_used) {
+            alpha = ex2_approx(m_used - m_tile);  // m_used = -inf gives 0
+            m_used = m_tile;
+          }
+        }
+        l *= alpha;
+      } else {
+        // Fast tiles keep m_used, so l (and O) grow with p <= 2^kFastLag.
+        // Past 2^32, m_used moves up by l's binary exponent e: l and O are
+        // multiplied by 2^-e exactly, and l stays above 1, so no term the sum
+        // depends on underflows.
+        if (__any_sync(0xffffffffu, l > 4294967296.f)) {
+          const int e = l > 4294967296.f ? ((__float_as_int(l) >> 23) & 0xFF) - 127 : 0;
+          alpha = __int_as_float((127 - e) << 23);  // 2^-e
+          m_used += (float)e;
+          l *= alpha;
         }
       }
-      l *= alpha;
+      TSK_EV(4);
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
       TSK_TRACE_T0(tr_exp);
       // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per element,
@@ -484,36 +556,39 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       uint32_t pk[64];
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm = f2_pack(-m_use, -m_use);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm), x0, x1);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        acc[c & 3] += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 64; ++c) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[c & 3] += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       }
-      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       TSK_TRACE_ADD(22, tr_exp);
       TSK_EV(5);
       if (j > 0) {
         // O_t is stable and P_t reusable once PV_t(j-1) has completed.
-        ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
-        if (!ok) break;
+        if (!mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort)) return false;
         TSK_EV(6);
         ++pv_cnt;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          uint32_t o[64];
-          tmem_ld_32x32b_x32(tO, o);
-          tmem_ld_32x32b_x32(tO + 32, o + 32);
-          tmem_wait_ld();
-          reg_fence<64>(o);
+        {
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            uint32_t o[64];
+            tmem_ld_32x32b_x32(tO, o);
+            tmem_ld_32x32b_x32(tO + 32, o + 32);
+            tmem_wait_ld();
+            reg_fence<64>(o);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st_32x32b_x32(tO, o);
-          tmem_st_32x32b_x32(tO + 32, o + 32);
+            for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st_32x32b_x32(tO, o);
+            tmem_st_32x32b_x32(tO + 32, o + 32);
+          }
         }
       }
       TSK_TRACE_T0(tr_st);
@@ -525,7 +600,16 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
       TSK_EV(7);
+      return true;
+    };
+    int j = 0;
+    // Tiles with the row maximum until the bound makes it unnecessary (with a
+    // sink, usually none), then tiles without it.
+    for (; j < n_kv && ok; ++j) {
+      if (__all_sync(0xffffffffu, m_used != -INFINITY && bq - m_used <= kFastLag)) break;
+      ok = step(j, SlowTile{});
     }
+    for (; j < n_kv && ok; ++j) ok = step(j, FastTile{});
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
     TSK_EV(9);
@@ -551,6 +635,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     tmem_ld_32x32b_x32(tO + 32, o + 32);
     tmem_wait_ld();
     reg_fence<64>(o);
+    TSK_EV(12);
     const float inv = rcp_approx(l);
     uint32_t ob[32];
 #pragma unroll
@@ -559,11 +644,13 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     const int row = e.y + r;  // query row, relative to the sequence's first query
     const size_t orow = (size_t)(e.x + row) * p.Hq + h;
     if (p.lse && row < e.w) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    TSK_EV(13);
     if (e.y + wq * 32 + 32 <= e.w) {
       // The warp's 32 rows lie inside the sequence: stage them in this warp's
       // slice of the staging tile and store them with one TMA bulk store.
       if (lane == 0) bulk_wait_group_read0();  // the warp's previous store has read its slice
       __syncwarp();
+      TSK_EV(14);
       const uint32_t dst_row = epi + (uint32_t)r * 128u;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
@@ -571,6 +658,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
                      ob[4 * c + 2], ob[4 * c + 3]);
       fence_proxy_async_shared();
       __syncwarp();
+      TSK_EV(15);
       if (lane == 0) {
         tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, e.x + e.y + wq * 32);
         bulk_commit_group();
@@ -863,6 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  if (warp == 3 && p.knorm)
+    for (int g = lane; g < p.Hkv; g += 32) st_shared_f32(cx.sbase + kSmemNorm + 4u * g, __ldg(p.knorm + g));
   trace_init();
   trace_cta_start();
   tc_fence_before();

@@ -81,6 +81,11 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   uint32_t q_iter = 0, k_iss = 0, v_iss = 0;  // loads issued per buffer kind
   bool ok = true;
   TSK_TL_DECL;
+#ifdef TSK_L2_HINTS
+  // Q tiles are read once; K/V tiles are read again by the other units of
+  // their KV head, possibly much later: keep them in L2 ahead of Q and O.
+  const uint64_t pol_q = l2_evict_first(), pol_kv = l2_evict_last();
+#endif
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit<QS>(p, u);
@@ -89,8 +94,13 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     mbar_arrive_expect_tx(cx.bar(kBarQFull), w.ntiles * kTile);
     for (int t = 0; t < w.ntiles; ++t)
       for (int hf = 0; hf < 2; ++hf)
+#ifdef TSK_L2_HINTS
+        tma_load_3d_hint(cx.sbase + kSmemQ + t * kTile + hf * kHalf, tmQ, cx.bar(kBarQFull),
+                         64 * hf, tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t), pol_q);
+#else
         tma_load_3d(cx.sbase + kSmemQ + t * kTile + hf * kHalf, tmQ, cx.bar(kBarQFull), 64 * hf,
                     tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t));
+#endif
     TSK_EV(20);
     ++q_iter;
     for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -104,6 +114,12 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
         const uint32_t dst = cx.sbase + kSmemKV + s * 2 * kTile;
         mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTile);
         for (int hf = 0; hf < 2; ++hf)
+#ifdef TSK_L2_HINTS
+          if (p.kv.page_size == 0)
+            tma_load_3d_hint(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g,
+                             w.start_k + pos0, pol_kv);
+          else
+#endif
           tma_load_key_rows(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g, p.kv,
                             w.seq, w.start_k, pos0, Lk);
         TSK_EV(21);
@@ -117,6 +133,12 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
         const uint32_t dst = cx.sbase + kSmemKV + s * 2 * kTile + kTile;
         mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kTile);
         for (int hf = 0; hf < 2; ++hf)
+#ifdef TSK_L2_HINTS
+          if (p.kv.page_size == 0)
+            tma_load_3d_hint(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g,
+                             w.start_k + pos0, pol_kv);
+          else
+#endif
           tma_load_key_rows(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g, p.kv,
                             w.seq, w.start_k, pos0, Lk);
         TSK_EV(22);
@@ -403,7 +425,11 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
+#ifdef TSK_L2_HINTS
+          tma_store_3d_hint(tmO, slice, 64 * hf, h, e.x + e.y + wq * 32, l2_evict_first());
+#else
           tma_store_3d(tmO, slice, 64 * hf, h, e.x + e.y + wq * 32);
+#endif
           bulk_commit_group();
         }
       } else if (row < e.w) {

@@ -21,8 +21,25 @@ constexpr int kTileN = 128;      // keys per tile
 // Workspace words (int32) at the head of the per-stream workspace.
 constexpr int kWsStatus = 0;   // [0] error code, [1] site, [2] block
 constexpr int kWsNTiles = 4;   // number of query tiles in the list
+constexpr int kWsNormCount = 5;  // key-norm blocks finished (reset by the last one)
 constexpr int kWsDecodeBad = 6;  // decode: this call's offset check
 constexpr int kWsHeader = 8;   // ints; tile offsets follow, then the int4 list (16-B aligned)
+
+// Key-norm pre-pass (extra blocks of the scheduler launch): the largest
+// Euclidean norm of the key rows of every KV head, max_t ||k[t, g, :]||, which
+// bounds every score of a query row q by ||q|| * max||k||.  Run for at most
+// kNormMaxHeads KV heads by at most kNormBlocks blocks; its buffer holds
+// kNormBlocks * kNormMaxHeads per-block maxima, then kNormMaxHeads results.
+constexpr int kNormBlocks = 32;
+constexpr int kNormMaxHeads = 256;
+constexpr int kNormFloats = (kNormBlocks + 1) * kNormMaxHeads;
+
+struct KeyNorms {
+  const uint4* k;  // key rows: [rows, heads, D] bf16, or nullptr (no pre-pass)
+  long long rows;  // rows of the key buffer (tokens, or pool slots of a paged cache)
+  int heads, D;
+  float* out;      // kNormFloats floats
+};
 
 // One query tile: two int4 per entry,
 //   {start_q, q0, kv_lo, len_q}  query start row, first query row of the tile
@@ -64,16 +81,75 @@ __device__ __forceinline__ bool pages_ok(const PagedKV& pg, int s, int Lk) {
   return true;
 }
 
+// Blocks 1.. of the scheduler launch: per-head maxima of key-row norms over
+// a grid-stride share of the rows; the last block to finish reduces the
+// per-block maxima and resets the counter.  Norms are non-negative, so their
+// bit patterns order like the values (shared-memory integer maxima); a NaN
+// norm orders above every finite one and disables the bound for its head.
+__device__ void key_norm_blocks(const KeyNorms& kn, int* __restrict__ ws, int* s_max,
+                                int* s_last, int blk, int nblk) {
+  const int tid = threadIdx.x;
+  for (int g = tid; g < kn.heads; g += kSchedThreads) s_max[g] = 0;
+  __syncthreads();
+  const long long total = kn.rows * kn.heads;
+  const int chunks = kn.D / 8;  // 16-byte chunks of a row
+  for (long long r = (long long)blk * kSchedThreads + tid; r < total;
+       r += (long long)nblk * kSchedThreads) {
+    const uint4* row = kn.k + r * chunks;
+    float acc = 0.f;
+    for (int c = 0; c < chunks; ++c) {
+      const uint4 v = __ldg(row + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+        acc = fmaf(lo, lo, acc);
+        acc = fmaf(hi, hi, acc);
+      }
+    }
+    atomicMax(&s_max[(int)(r % kn.heads)], __float_as_int(sqrtf(acc)));
+  }
+  __syncthreads();
+  for (int g = tid; g < kn.heads; g += kSchedThreads)
+    kn.out[blk * kNormMaxHeads + g] = __int_as_float(s_max[g]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) *s_last = atomicAdd(&ws[kWsNormCount], 1) == nblk - 1;
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    for (int g = tid; g < kn.heads; g += kSchedThreads) {
+      int m = 0;
+      for (int b = 0; b < nblk; ++b)
+        m = max(m, __float_as_int(__ldcg(kn.out + b * kNormMaxHeads + g)));
+      kn.out[kNormBlocks * kNormMaxHeads + g] = __int_as_float(m);
+    }
+    if (tid == 0) ws[kWsNormCount] = 0;
+  }
+}
+
+// The key-norm pre-pass alone (gridDim.x <= kNormBlocks blocks); ws[kWsNormCount]
+// must be zero at launch (the last block resets it).
+__global__ void __launch_bounds__(kSchedThreads, 1) key_norm_kernel(KeyNorms kn, int* ws) {
+  __shared__ int s_max[kNormMaxHeads];
+  __shared__ int s_last;
+  key_norm_blocks(kn, ws, s_max, &s_last, blockIdx.x, gridDim.x);
+}
+
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k,
                     int num_seqs, int total_tokens, int total_keys, int window,
                     int* __restrict__ ws, int* __restrict__ tile_off, int4* __restrict__ list,
-                    int max_tiles, PagedKV pg, int entry_rows) {
+                    int max_tiles, PagedKV pg, int entry_rows, KeyNorms kn) {
   __shared__ int s_scan[kSchedThreads];
   __shared__ int s_hist[kCostBins];
   __shared__ int s_cursor[kCostBins];
   __shared__ int s_bad, s_base;
   const int tid = threadIdx.x;
+  if (blockIdx.x > 0) {
+    key_norm_blocks(kn, ws, s_hist, &s_bad, blockIdx.x - 1, gridDim.x - 1);
+    return;
+  }
   if (tid == 0) {
     s_bad = (cu[0] != 0 || cu[num_seqs] != total_tokens || cu_k[0] != 0 ||
              cu_k[num_seqs] != total_keys) ? 1 : 0;

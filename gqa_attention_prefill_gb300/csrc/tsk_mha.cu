@@ -198,7 +198,7 @@ tsk_status get_workspace(int dev, cudaStream_t stream, int max_tiles, int num_se
   mt = mt < 1024 ? 1024 : mt;
   ms = ms < 1024 ? 1024 : ms;
   size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ms + 1 + 3) & ~(size_t)3;
-  size_t bytes = off_ints * 4 + (size_t)mt * 4 * tsk::kTileEntryInts;
+  size_t bytes = off_ints * 4 + (size_t)mt * 4 * tsk::kTileEntryInts + tsk::kNormFloats * 4;
   int* nb = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -341,6 +341,18 @@ void launch_attention(int D, int window, int qstep, int grid, const CUtensorMap&
   else launch_attention_qs<0>(D, window, grid, tq, tk, tv, to, p, stream);
 }
 
+// The key-norm pre-pass (extra scheduler blocks) for a D = 64 prefill: the
+// kernel bounds every score of a row by its query norm times the largest
+// key norm of the KV head and skips the row maximum while that bound allows
+// it.  Returns the number of extra blocks (0: no bound; too many KV heads).
+int key_norm_setup(tsk::KeyNorms* kn, const void* k, int64_t rows, int Hkv, int D, float* out) {
+  *kn = tsk::KeyNorms{nullptr, 0, 0, 0, nullptr};
+  if (D != 64 || Hkv > tsk::kNormMaxHeads || rows <= 0) return 0;
+  *kn = tsk::KeyNorms{reinterpret_cast<const uint4*>(k), (long long)rows, Hkv, D, out};
+  const int64_t want = (rows * Hkv + 8 * tsk::kSchedThreads - 1) / (8 * tsk::kSchedThreads);
+  return (int)(want < tsk::kNormBlocks ? (want < 1 ? 1 : want) : tsk::kNormBlocks);
+}
+
 // Shared by tsk_mha_prefill (cu_k == cu_q, total_keys == total_queries) and
 // tsk_mha_prefill_kvcache.
 // Host checks of a paged cache description; rows = cache rows it spans.
@@ -361,7 +373,8 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
                         int64_t total_q, int64_t total_k, int32_t Hq, int32_t Hkv, int32_t D,
                         int32_t window, float scale, void* out, float* lse,
                         cudaStream_t stream, const char* what, const int32_t* block_table = nullptr,
-                        int32_t max_blocks = 0, int32_t page_size = 0, int32_t num_pages = 0) {
+                        int32_t max_blocks = 0, int32_t page_size = 0, int32_t num_pages = 0,
+                        const float* knorm_ext = nullptr) {
   // ---- host-only checks (no CUDA call before these pass)
   if (!q || !k || !v || !out || !cu_q || !cu_k) return TSK_ERR_INVALID_ARG;
   if (num_seqs < 0 || total_q < 0 || total_k < 0 || Hq <= 0 || Hkv <= 0)
@@ -437,9 +450,14 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   // With one query head per KV head, a unit takes two consecutive 128-row
   // tiles of one head (list entries of 256 rows); else two heads of a group.
   const int qstep = Hq == Hkv ? tsk::kTileM : 0;
-  tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
+  float* knorm = reinterpret_cast<float*>(ws->base + off_ints + (size_t)ws->max_tiles * tsk::kTileEntryInts);
+  tsk::KeyNorms kn;
+  // (knorm_ext: bounds the caller computed over a larger key set)
+  const int norm_blocks = knorm_ext ? 0 : key_norm_setup(&kn, k, kv_rows, Hkv, D, knorm);
+  if (knorm_ext) kn = tsk::KeyNorms{nullptr, 0, 0, 0, nullptr};
+  tsk::schedule_kernel<<<1 + norm_blocks, tsk::kSchedThreads, 0, stream>>>(
       cu_q, cu_k, num_seqs, (int)total_q, (int)total_k, window, ws->base, tile_off, list,
-      ws->max_tiles, pg, tsk::kTileM + qstep);
+      ws->max_tiles, pg, tsk::kTileM + qstep, kn);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
   tsk::AttnParams p;
@@ -458,6 +476,8 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = g_debug_stall;
   p.kv = pg;
+  p.knorm = knorm_ext ? knorm_ext
+                      : norm_blocks ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   launch_attention(D, window, qstep, grid, tq, tk, tv, to, p, stream);
@@ -607,8 +627,9 @@ constexpr int kNoAllocMaxSeqs = 16384;    // sequences per call
 constexpr int kNoAllocMaxTiles = 49152;   // total_tokens/128 + num_seqs + 1, at most
 constexpr size_t kNoAllocOffInts =
     ((size_t)tsk::kWsHeader + (size_t)kNoAllocMaxSeqs + 1 + 3) & ~(size_t)3;
-constexpr size_t kNoAllocBytes =
-    kNoAllocOffInts * 4 + (size_t)kNoAllocMaxTiles * 4 * tsk::kTileEntryInts;  // ~1.6 MB
+constexpr size_t kNoAllocBytes = kNoAllocOffInts * 4 +
+                                 (size_t)kNoAllocMaxTiles * 4 * tsk::kTileEntryInts +
+                                 tsk::kNormFloats * 4;  // ~1.6 MB
 
 static __device__ __align__(256) int g_noalloc_scratch[kNoAllocBytes / 4];
 
@@ -679,9 +700,13 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   cudaError_t e = cudaMemsetAsync(scratch, 0, tsk::kWsHeader * sizeof(int), stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch header");
   const int qstep = Hq == Hkv ? tsk::kTileM : 0;  // see prefill_impl
-  tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
+  float* knorm = reinterpret_cast<float*>(scratch + kNoAllocOffInts +
+                                          (size_t)kNoAllocMaxTiles * tsk::kTileEntryInts);
+  tsk::KeyNorms kn;
+  const int norm_blocks = key_norm_setup(&kn, k, total_tokens, Hkv, D, knorm);
+  tsk::schedule_kernel<<<1 + norm_blocks, tsk::kSchedThreads, 0, stream>>>(
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, scratch,
-      tile_off, list, kNoAllocMaxTiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM + qstep);
+      tile_off, list, kNoAllocMaxTiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM + qstep, kn);
 
   tsk::AttnParams p;
   p.sinks = sinks;
@@ -699,6 +724,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = 0;
   p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
+  p.knorm = norm_blocks ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   launch_attention(D, window, qstep, grid, tq, tk, tv, to, p, stream);
@@ -1018,7 +1044,8 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   }
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, ws->base,
-      tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM);
+      tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM,
+      tsk::KeyNorms{nullptr, 0, 0, 0, nullptr});
   tsk::fp8::fp8_vt_kernel<<<dim3(max_tiles, Hkv), 128, 0, stream>>>(
       reinterpret_cast<const uint8_t*>(v8), cu_seqlens, tile_off, ws->base, num_seqs, Hkv, ws->vt,
       t_pad);
@@ -1178,7 +1205,8 @@ extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const v
   const size_t off_q = 0, off_k = align256(q_bytes), off_v = off_k + align256(kv_bytes),
                off_o = off_v + align256(kv_bytes), off_l = off_o + align256(q_bytes),
                off_s = off_l + align256(lse_bytes), off_c = off_s + align256(sink_bytes),
-               need = off_c + align256(cu_host.size() * 4);
+               off_n = off_c + align256(cu_host.size() * 4),
+               need = off_n + align256((tsk::kNormFloats + 8) * 4);
   if (hp.cap < need) {
     if (hp.buf) {
       cudaStreamSynchronize(stream);  // earlier calls on this stream may still use it
@@ -1213,6 +1241,19 @@ extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const v
     cudaMemcpyAsync(b + off_c, cu_host.data(), cu_host.size() * 4, cudaMemcpyHostToDevice, hp.h2d);
     const float* d_sinks = sinks ? reinterpret_cast<const float*>(b + off_s) : nullptr;
     const int32_t* d_cu = reinterpret_cast<const int32_t*>(b + off_c);
+    // The key-norm bound over all keys, as tsk_mha_prefill computes it, so
+    // that every chunk makes the same choices and the results stay bit for
+    // bit those of tsk_mha_prefill: K is copied whole first.
+    tsk::KeyNorms kn;
+    int* n_ws = reinterpret_cast<int*>(b + off_n);  // [kWsNormCount] counter, then the norms
+    float* n_out = reinterpret_cast<float*>(b + off_n) + 8;
+    const int nb = key_norm_setup(&kn, b + off_k, T, Hkv, D, n_out);
+    const float* d_knorm = nb ? n_out + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
+    if (nb) {
+      cudaMemcpyAsync(b + off_k, k, T * kvrow, cudaMemcpyHostToDevice, hp.h2d);
+      cudaMemsetAsync(n_ws, 0, 8 * sizeof(int), hp.h2d);
+      tsk::key_norm_kernel<<<nb, tsk::kSchedThreads, 0, hp.h2d>>>(kn, n_ws);
+    }
     for (size_t c = 0; c < chunks.size() && st == TSK_OK; ++c) {
       const HostChunk& ch = chunks[c];
       const int64_t n = ch.t1 - ch.t0;
@@ -1225,7 +1266,7 @@ extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const v
       const uint8_t* hk = static_cast<const uint8_t*>(k) + ch.t0 * kvrow;
       const uint8_t* hv = static_cast<const uint8_t*>(v) + ch.t0 * kvrow;
       cudaMemcpyAsync(b + off_q + ch.t0 * qrow, hq, n * qrow, cudaMemcpyHostToDevice, hp.h2d);
-      cudaMemcpyAsync(b + off_k + ch.t0 * kvrow, hk, n * kvrow, cudaMemcpyHostToDevice, hp.h2d);
+      if (!nb) cudaMemcpyAsync(b + off_k + ch.t0 * kvrow, hk, n * kvrow, cudaMemcpyHostToDevice, hp.h2d);
       cudaMemcpyAsync(b + off_v + ch.t0 * kvrow, hv, n * kvrow, cudaMemcpyHostToDevice, hp.h2d);
       cudaEventRecord(ev_in, hp.h2d);
       cudaStream_t cs = hp.comp[c & 1];
@@ -1236,7 +1277,7 @@ extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const v
                           d_cu + ch.cu_off + ch.nseq + 1, ch.nseq, n, ch.t1 - ch.k0, Hq, Hkv, D,
                           window, scale, b + off_o + ch.t0 * qrow,
                           lse ? reinterpret_cast<float*>(b + off_l) + ch.t0 * Hq : nullptr, cs,
-                          "tsk_mha_prefill_host");
+                          "tsk_mha_prefill_host", nullptr, 0, 0, 0, d_knorm);
       }
       cudaEventRecord(ev_out, cs);
       cudaStreamWaitEvent(hp.d2h, ev_out, 0);

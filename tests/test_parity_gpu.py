@@ -56,6 +56,24 @@ def test_extreme_sinks_and_scales():
     print(parity.check_full(w, label="peaky K x4"))
 
 
+@pytest.mark.parametrize("sink", [-30.0, 30.0])
+def test_sinks_far_from_the_scores(sink):
+    # Sinks far below the scores: key tiles that skip the row maximum keep the
+    # sink as the reference, so the running sum grows past 2^32 and is
+    # renormalised by powers of two.  Far above: every p is tiny next to the
+    # sink's term.
+    w = inputgen.make([700, 1300, 64], 8, 2, seed=41)
+    w.sinks = np.full(w.Hq, sink, dtype=np.float32)
+    print(parity.check_full(w, label=f"sinks {sink}"))
+
+
+def test_scores_beyond_the_key_norm_bound():
+    # |q| |k| scale far above the scores' spread: the bound never allows
+    # skipping the row maximum (every tile computes it)
+    w = inputgen.make([500, 129], 8, 2, seed=42, k_mult=16.0, scale=0.5)
+    print(parity.check_full(w, label="no fast tiles"))
+
+
 def test_window_config_full():
     print(parity.check_full(inputgen.config("window128_4x4096_h64kv8")))
 
