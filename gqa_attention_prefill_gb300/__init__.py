@@ -34,7 +34,7 @@ _lib = None
 
 STATUS = {0: "TSK_OK", -1: "TSK_ERR_INVALID_ARG", -2: "TSK_ERR_UNSUPPORTED",
           -3: "TSK_ERR_ALIGNMENT", -4: "TSK_ERR_DEVICE", -5: "TSK_ERR_OOM", -6: "TSK_ERR_LAUNCH",
-          -7: "TSK_ERR_DEVICE_TIMEOUT", -8: "TSK_ERR_BAD_SEQLENS"}
+          -7: "TSK_ERR_DEVICE_TIMEOUT", -8: "TSK_ERR_BAD_SEQLENS", -9: "TSK_ERR_BOUNDS"}
 
 
 class TskError(RuntimeError):
@@ -113,6 +113,8 @@ def load_library():
         lib.tsk_kernels_per_call.restype = i32
         lib.tsk_release.argtypes = []
         lib.tsk_release.restype = ctypes.c_int
+        lib.tsk_debug_shrink_extent.argtypes = [i32]
+        lib.tsk_debug_shrink_extent.restype = ctypes.c_int
         lib.tsk_debug_set_wait.argtypes = [ctypes.c_ulonglong, ctypes.c_int]
         lib.tsk_debug_set_wait.restype = ctypes.c_int
         lib.tsk_version.argtypes = []
@@ -379,6 +381,11 @@ def tsk_bench_ex2_rate(stream=None) -> float:
     if rc != 0:
         raise TskError(rc, "tsk_bench_ex2_rate")
     return r.value
+
+
+def tsk_debug_shrink_extent(rows: int) -> int:
+    """Test hook of -DTSK_DEBUG builds (TSK_ERR_UNSUPPORTED otherwise)."""
+    return load_library().tsk_debug_shrink_extent(int(rows))
 
 
 def tsk_kernels_per_call() -> int:

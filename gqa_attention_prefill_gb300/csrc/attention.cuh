@@ -92,6 +92,9 @@ struct AttnParams {
   int debug_stall;      // test hook: producer first waits on a barrier nothing signals
   PagedKV kv;           // paged key/value cache, or kv.page_size == 0 (contiguous)
   const float* knorm = nullptr;  // [Hkv] largest key-row norm per KV head, or nullptr
+  // Extents checked by builds with -DTSK_DEBUG: rows of q/out, rows of the
+  // k/v buffers (tokens, or slots of a paged pool), capacity of the tile list.
+  int q_rows = 0, kv_rows = 0, max_tiles = 0;
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.
@@ -133,8 +136,9 @@ struct Unit {
 template <int QS = 0>
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
   const int per_tile = p.Hkv * p.HP;
-  const int qi = u / per_tile;
+  int qi = u / per_tile;
   const int rem = u - qi * per_tile;
+  if (!TSK_IN_BOUNDS(p, 0u, qi < p.max_tiles, 40)) qi = 0;  // (the unit is then wrong, the status says so)
   const int4 e = __ldg(p.list + 2 * qi);
   const int4 f = __ldg(p.list + 2 * qi + 1);
   Unit r;
@@ -181,27 +185,38 @@ __device__ __forceinline__ int4 ld_nc_v4_volatile(const int4* a) {
 // swizzle is that of a single box); chunks past the sequence's last page
 // re-read that page (their keys are masked).  Out of line: it is rare next to
 // the contiguous case and stays out of the kernels' hot code.
-__device__ __noinline__ void tma_load_key_rows_paged(uint32_t dst, const CUtensorMap* tm,
+// In builds with -DTSK_DEBUG a page outside the pool is not loaded and the
+// function returns false.
+__device__ __noinline__ bool tma_load_key_rows_paged(uint32_t dst, const CUtensorMap* tm,
                                                      uint32_t bar, int x, int head,
                                                      const PagedKV pg, int seq, int pos0, int Lk) {
   const int chunk = pg.page_size < 128 ? pg.page_size : 128;
   const int last_blk = (Lk - 1) / pg.page_size;
+  bool in_pool = true;
   for (int c = 0; c < 128; c += chunk) {
     const int pos = pos0 + c;
     int blk = pos / pg.page_size;
     if (blk > last_blk) blk = last_blk;
     const int page = __ldg(pg.table + (size_t)seq * pg.max_blocks + blk);
+#ifdef TSK_DEBUG
+    if (page < 0 || page >= pg.num_pages || blk >= pg.max_blocks) {
+      in_pool = false;
+      continue;
+    }
+#endif
     tma_load_3d(dst + (uint32_t)c * 128u, tm, bar, x, head, page * pg.page_size + pos % pg.page_size);
   }
+  return in_pool;
 }
 
 // The same for either cache layout; a contiguous cache (page_size 0) is one
 // box at row row0 + pos0.
-__device__ __forceinline__ void tma_load_key_rows(uint32_t dst, const CUtensorMap* tm,
+__device__ __forceinline__ bool tma_load_key_rows(uint32_t dst, const CUtensorMap* tm,
                                                   uint32_t bar, int x, int head, const PagedKV& pg,
                                                   int seq, int row0, int pos0, int Lk) {
-  if (pg.page_size == 0) tma_load_3d(dst, tm, bar, x, head, row0 + pos0);
-  else tma_load_key_rows_paged(dst, tm, bar, x, head, pg, seq, pos0, Lk);
+  if (pg.page_size != 0) return tma_load_key_rows_paged(dst, tm, bar, x, head, pg, seq, pos0, Lk);
+  tma_load_3d(dst, tm, bar, x, head, row0 + pos0);
+  return true;
 }
 
 // State shared by the roles of one CTA.
@@ -235,9 +250,16 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, 1, p, cx.abort);
     if (!ok) break;
     mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), w.ntiles * kTileBytes);
-    for (int t = 0; t < w.ntiles; ++t)
+    for (int t = 0; t < w.ntiles; ++t) {
+      const int h = tile_head<QS>(w, t), row = w.start + tile_q0<QS>(w, t);
+      if (!TSK_IN_BOUNDS(p, cx.abort, h >= 0 && h < p.Hq && row >= 0 && row < p.q_rows, 41)) {
+        ok = false;
+        break;
+      }
       tma_load_3d(cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes, tmQ, cx.bar(kBarQFull + qb), 0,
-                  tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t));
+                  h, row);
+    }
+    if (!ok) break;
     ++q_iter;
     for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
       const int s = kv_iter % kStages;
@@ -248,11 +270,24 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
       const int pos0 = (w.kv_lo + j) * kTileN;  // key position of the tile's first key
       const int Lk = w.offset + w.len;
       const uint32_t kdst = cx.sbase + kSmemKV + s * 2 * kTileBytes;
+      if (!TSK_IN_BOUNDS(p, cx.abort,
+                         w.g >= 0 && w.g < p.Hkv &&
+                             (p.kv.page_size != 0 ||
+                              (w.start_k + pos0 >= 0 && w.start_k + pos0 < p.kv_rows)),
+                         42)) {
+        ok = false;
+        break;
+      }
       mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTileBytes);
-      tma_load_key_rows(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, p.kv, w.seq, w.start_k, pos0, Lk);
+      bool in = tma_load_key_rows(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, p.kv, w.seq, w.start_k,
+                                  pos0, Lk);
       mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kTileBytes);
-      tma_load_key_rows(kdst + kTileBytes, tmV, cx.bar(kBarVFull + s), 0, w.g, p.kv, w.seq,
-                        w.start_k, pos0, Lk);
+      in = tma_load_key_rows(kdst + kTileBytes, tmV, cx.bar(kBarVFull + s), 0, w.g, p.kv, w.seq,
+                             w.start_k, pos0, Lk) && in;
+      if (!TSK_IN_BOUNDS(p, cx.abort, in, 43)) {
+        ok = false;
+        break;
+      }
     }
   }
   // Drain: wait for the last load issued into every buffer so that no
@@ -411,29 +446,45 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   TSK_TL_DECL;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
+  // What the key loop needs from a unit (the epilogue reads the sequence
+  // fields again: registers are the scarce resource here).  The next unit's
+  // fields are loaded before a unit's epilogue, so that their latency passes
+  // while the epilogue waits for the last PV.
+  struct Fields {
+    int n_kv, kv_lo, diag0, gk;
+    float sink;  // sink * log2(e), or -inf
+    bool active;
+  };
+  auto fetch = [&](int uu) {
+    Fields f{0, 0, 0, 0, -INFINITY, false};
+    if (uu < cx.total_units) {
+      const Unit w = decode_unit<QS>(p, uu);
+      f.active = t < w.ntiles;
+      f.gk = w.g;
+      f.n_kv = w.n_kv;
+      f.kv_lo = w.kv_lo;
+      f.diag0 = w.offset + tile_q0<QS>(w, t);  // key position of the tile's first query row
+      if (p.sinks && f.active &&
+          TSK_IN_BOUNDS(p, cx.abort, tile_head<QS>(w, t) >= 0 && tile_head<QS>(w, t) < p.Hq, 44))
+        f.sink = __ldg(p.sinks + tile_head<QS>(w, t)) * 1.4426950408889634f;
+    }
+    return f;
+  };
+  Fields nx = fetch(blockIdx.x);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     TSK_EV(8);
     TSK_TRACE_T0(tr_dec);
-    // Only what the key loop needs is kept from the unit; the epilogue reads
-    // the sequence fields again (registers are the scarce resource here).
-    int n_kv, kv_lo, diag0, pos, gk;
-    float m_used = -INFINITY, l = 0.f;
     const int qb = q_iter & 1;
     const uint32_t q_par = (q_iter >> 1) & 1;
     ++q_iter;
-    {
-      const Unit w = decode_unit<QS>(p, u);
-      if (t >= w.ntiles) continue;
-      gk = w.g;
-      n_kv = w.n_kv;
-      kv_lo = w.kv_lo;
-      diag0 = w.offset + tile_q0<QS>(w, t);  // key position of the tile's first query row
-      pos = diag0 + r;                      // key position of this thread's query row
-      if (p.sinks) {
-        m_used = __ldg(p.sinks + tile_head<QS>(w, t)) * 1.4426950408889634f;
-        l = 1.f;
-      }
+    const Fields cf = nx;
+    if (!cf.active) {
+      nx = fetch(u + gridDim.x);
+      continue;
     }
+    const int n_kv = cf.n_kv, kv_lo = cf.kv_lo, diag0 = cf.diag0, gk = cf.gk;
+    const int pos = diag0 + r;  // key position of this thread's query row
+    float m_used = cf.sink, l = cf.sink == -INFINITY ? 0.f : 1.f;
     TSK_TRACE_ADD(24, tr_dec);
     // Bound on x = s * scale * log2(e) for every key of this row: ||q|| times
     // the largest key norm of the KV head (Cauchy-Schwarz).
@@ -445,7 +496,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       TSK_EV(18);
       // the row's 128 bytes (8 chunks of 16, permuted by the swizzle)
       const uint32_t qrow = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes + (uint32_t)r * 128u;
-      float ss = 0.f;
+      float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         // chunk k ^ (r & 7): the lanes of a warp spread over all 32 banks
@@ -454,11 +505,12 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-          ss = fmaf(lo, lo, ss);
-          ss = fmaf(hi, hi, ss);
+          ss[2 * e] = fmaf(lo, lo, ss[2 * e]);
+          ss[2 * e + 1] = fmaf(hi, hi, ss[2 * e + 1]);
         }
       }
-      bq = sl2 * sqrtf(ss) * cx.knorm_smem(gk);
+      const float sq = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
+      bq = sl2 * sqrtf(sq) * cx.knorm_smem(gk);
       TSK_EV(19);
     }
     // One key tile.  A slow tile computes its row maximum and raises the
@@ -611,6 +663,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     }
     for (; j < n_kv && ok; ++j) ok = step(j, FastTile{});
     if (!ok) break;
+    nx = fetch(u + gridDim.x);
     // ------------------------------------------------------------ epilogue
     TSK_EV(9);
     const int per_tile = p.Hkv * p.HP;
@@ -637,13 +690,20 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     reg_fence<64>(o);
     TSK_EV(12);
     const float inv = rcp_approx(l);
+    const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t ob[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
-      ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+    for (int c = 0; c < 32; ++c) {
+      float a, b;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1])), inv2),
+                a, b);
+      ob[c] = pack_bf16x2(a, b);
+    }
     const int row = e.y + r;  // query row, relative to the sequence's first query
     const size_t orow = (size_t)(e.x + row) * p.Hq + h;
-    if (p.lse && row < e.w) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    // (rows past the sequence's end are neither stored nor checked)
+    const bool row_ok = row < e.w && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
+    if (p.lse && row_ok) p.lse[orow] = (m_used + lg2_approx(l)) * 0.69314718055994531f;
     TSK_EV(13);
     if (e.y + wq * 32 + 32 <= e.w) {
       // The warp's 32 rows lie inside the sequence: stage them in this warp's
@@ -659,11 +719,12 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       fence_proxy_async_shared();
       __syncwarp();
       TSK_EV(15);
-      if (lane == 0) {
+      if (lane == 0 && TSK_IN_BOUNDS(p, cx.abort,
+                                     h < p.Hq && e.x + e.y + wq * 32 + 32 <= p.q_rows, 46)) {
         tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, e.x + e.y + wq * 32);
         bulk_commit_group();
       }
-    } else if (row < e.w) {
+    } else if (row_ok) {
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
 #pragma unroll
       for (int c = 0; c < 8; ++c)
@@ -710,7 +771,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     const int row = q0t + r;           // query row, relative to the sequence's first query
     const int pos = w.offset + row;    // its key position
     float m_used = -INFINITY, l = 0.f;
-    if (p.sinks) {
+    if (p.sinks && TSK_IN_BOUNDS(p, cx.abort, h >= 0 && h < p.Hq, 44)) {
       m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
       l = 1.f;
     }
@@ -870,7 +931,9 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     for (int c = 0; c < 32; ++c)
       ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
     const size_t orow = (size_t)(w.start + row) * p.Hq + h;
-    if (p.lse && row < w.len) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    // (rows past the sequence's end are neither stored nor checked)
+    const bool row_ok = row < w.len && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
+    if (p.lse && row_ok) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
     if (q0t + wq * 32 + 32 <= w.len) {
       // The warp's 32 rows lie inside the sequence: stage them in this warp's
       // slice of the staging tile and store them with one TMA bulk store.
@@ -883,11 +946,12 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
                      ob[4 * c + 2], ob[4 * c + 3]);
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && TSK_IN_BOUNDS(p, cx.abort,
+                                     h < p.Hq && w.start + q0t + wq * 32 + 32 <= p.q_rows, 46)) {
         tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, w.start + q0t + wq * 32);
         bulk_commit_group();
       }
-    } else if (row < w.len) {
+    } else if (row_ok) {
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
 #pragma unroll
       for (int c = 0; c < 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);

@@ -81,26 +81,23 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   uint32_t q_iter = 0, k_iss = 0, v_iss = 0;  // loads issued per buffer kind
   bool ok = true;
   TSK_TL_DECL;
-#ifdef TSK_L2_HINTS
-  // Q tiles are read once; K/V tiles are read again by the other units of
-  // their KV head, possibly much later: keep them in L2 ahead of Q and O.
-  const uint64_t pol_q = l2_evict_first(), pol_kv = l2_evict_last();
-#endif
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit<QS>(p, u);
     if (q_iter >= 1) ok = mbar_wait(cx.bar(kBarQEmpty), (q_iter - 1) & 1, 1, p, cx.abort);
     if (!ok) break;
     mbar_arrive_expect_tx(cx.bar(kBarQFull), w.ntiles * kTile);
-    for (int t = 0; t < w.ntiles; ++t)
+    for (int t = 0; t < w.ntiles && ok; ++t) {
+      const int h = tile_head<QS>(w, t), row = w.start + tile_q0<QS>(w, t);
+      if (!TSK_IN_BOUNDS(p, cx.abort, h >= 0 && h < p.Hq && row >= 0 && row < p.q_rows, 41)) {
+        ok = false;
+        break;
+      }
       for (int hf = 0; hf < 2; ++hf)
-#ifdef TSK_L2_HINTS
-        tma_load_3d_hint(cx.sbase + kSmemQ + t * kTile + hf * kHalf, tmQ, cx.bar(kBarQFull),
-                         64 * hf, tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t), pol_q);
-#else
         tma_load_3d(cx.sbase + kSmemQ + t * kTile + hf * kHalf, tmQ, cx.bar(kBarQFull), 64 * hf,
-                    tile_head<QS>(w, t), w.start + tile_q0<QS>(w, t));
-#endif
+                    h, row);
+    }
+    if (!ok) break;
     TSK_EV(20);
     ++q_iter;
     for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -112,16 +109,23 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
         if (k >= 1) ok = mbar_wait(cx.bar(kBarKEmpty + s), (k - 1) & 1, 2, p, cx.abort);
         if (!ok) break;
         const uint32_t dst = cx.sbase + kSmemKV + s * 2 * kTile;
+        if (!TSK_IN_BOUNDS(p, cx.abort,
+                           w.g >= 0 && w.g < p.Hkv &&
+                               (p.kv.page_size != 0 ||
+                                (w.start_k + pos0 >= 0 && w.start_k + pos0 < p.kv_rows)),
+                           42)) {
+          ok = false;
+          break;
+        }
         mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTile);
+        bool in = true;
         for (int hf = 0; hf < 2; ++hf)
-#ifdef TSK_L2_HINTS
-          if (p.kv.page_size == 0)
-            tma_load_3d_hint(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g,
-                             w.start_k + pos0, pol_kv);
-          else
-#endif
-          tma_load_key_rows(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g, p.kv,
-                            w.seq, w.start_k, pos0, Lk);
+          in = tma_load_key_rows(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g,
+                                 p.kv, w.seq, w.start_k, pos0, Lk) && in;
+        if (!TSK_IN_BOUNDS(p, cx.abort, in, 43)) {
+          ok = false;
+          break;
+        }
         TSK_EV(21);
         ++k_iss;
       }
@@ -132,15 +136,14 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
         if (!ok) break;
         const uint32_t dst = cx.sbase + kSmemKV + s * 2 * kTile + kTile;
         mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kTile);
+        bool in = true;
         for (int hf = 0; hf < 2; ++hf)
-#ifdef TSK_L2_HINTS
-          if (p.kv.page_size == 0)
-            tma_load_3d_hint(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g,
-                             w.start_k + pos0, pol_kv);
-          else
-#endif
-          tma_load_key_rows(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g, p.kv,
-                            w.seq, w.start_k, pos0, Lk);
+          in = tma_load_key_rows(dst + hf * kHalf, tmV, cx.bar(kBarVFull + s), 64 * hf, w.g,
+                                 p.kv, w.seq, w.start_k, pos0, Lk) && in;
+        if (!TSK_IN_BOUNDS(p, cx.abort, in, 43)) {
+          ok = false;
+          break;
+        }
         TSK_EV(22);
         ++v_iss;
       }
@@ -265,7 +268,8 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
       diag0 = w.offset + tile_q0<QS>(w, t);
       pos = diag0 + r;
       if (p.sinks) {
-        m_used = __ldg(p.sinks + tile_head<QS>(w, t)) * 1.4426950408889634f;
+        if (TSK_IN_BOUNDS(p, cx.abort, tile_head<QS>(w, t) >= 0 && tile_head<QS>(w, t) < p.Hq, 44))
+          m_used = __ldg(p.sinks + tile_head<QS>(w, t)) * 1.4426950408889634f;
         l = 1.f;
       }
     }
@@ -400,7 +404,9 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
     TSK_TRACE_T0(tr_epi);
     const int row = e.y + r;
     const size_t orow = (size_t)(e.x + row) * p.Hq + h;
-    if (p.lse && row < e.w) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    // (rows past the sequence's end are neither stored nor checked)
+    const bool row_ok = row < e.w && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
+    if (p.lse && row_ok) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
     const float inv = rcp_approx(l);
     const bool staged = e.y + wq * 32 + 32 <= e.w;
 #pragma unroll
@@ -424,15 +430,12 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
                        ob[4 * c + 2], ob[4 * c + 3]);
         fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0) {
-#ifdef TSK_L2_HINTS
-          tma_store_3d_hint(tmO, slice, 64 * hf, h, e.x + e.y + wq * 32, l2_evict_first());
-#else
+        if (lane == 0 && TSK_IN_BOUNDS(p, cx.abort,
+                                       h < p.Hq && e.x + e.y + wq * 32 + 32 <= p.q_rows, 46)) {
           tma_store_3d(tmO, slice, 64 * hf, h, e.x + e.y + wq * 32);
-#endif
           bulk_commit_group();
         }
-      } else if (row < e.w) {
+      } else if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kD + 64 * hf);
 #pragma unroll
         for (int c = 0; c < 8; ++c)

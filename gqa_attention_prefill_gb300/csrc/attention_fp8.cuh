@@ -99,6 +99,9 @@ struct Fp8Params {
   AttnParams a;         // as the bf16 kernels (out, lse, list, ws, status, heads, window)
   const int* tile_off;  // [num_seqs + 1] query tiles before each sequence (schedule)
   float v_scale;
+  // Extents checked by builds with -DTSK_DEBUG: sequences, V^T columns (keys).
+  int num_seqs = 0;
+  long long vt_cols = 0;
 };
 
 // Transposed V: vt[g][d][128 * i + r] = v[key r of query tile i][g][d] (zero
@@ -110,6 +113,15 @@ __global__ void __launch_bounds__(128)
   __shared__ __align__(16) uint8_t tile[128][64 + 16];
   const int i = blockIdx.x, g = blockIdx.y;
   if (i >= ws[kWsNTiles]) return;
+#ifdef TSK_DEBUG
+  if ((int64_t)(i + 1) * 128 > t_pad) {  // V^T too narrow for the tile list
+    if (atomicCAS(const_cast<int*>(ws) + kWsStatus, 0, -9) == 0) {
+      const_cast<int*>(ws)[kWsStatus + 1] = 50;
+      const_cast<int*>(ws)[kWsStatus + 2] = (int)blockIdx.x;
+    }
+    return;
+  }
+#endif
   int lo = 0, hi = num_seqs - 1;  // the sequence owning tile i
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -158,10 +170,18 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, 1, p, cx.abort);
     if (!ok) break;
     mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), w.ntiles * kQTile);
-    for (int t = 0; t < w.ntiles; ++t)
+    for (int t = 0; t < w.ntiles; ++t) {
+      if (!TSK_IN_BOUNDS(p, cx.abort,
+                         w.h0 + t < p.Hq && w.start + w.q0 >= 0 && w.start + w.q0 < p.q_rows, 41)) {
+        ok = false;
+        break;
+      }
       tma_load_3d(cx.sbase + kSmemQ + (2 * qb + t) * kQTile, tmQ, cx.bar(kBarQFull + qb), 0,
                   w.h0 + t, w.start + w.q0);
+    }
+    if (!ok) break;
     ++q_iter;
+    if (!TSK_IN_BOUNDS(p, cx.abort, w.seq >= 0 && w.seq < f.num_seqs, 47)) break;
     const int vt_tile0 = __ldg(f.tile_off + w.seq);  // the sequence's first tile in V^T
     for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
       const int s = kv_iter % kStages;
@@ -170,6 +190,13 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
       if (!ok) break;
       const int kt = w.kv_lo + j;
       const uint32_t kdst = cx.sbase + kSmemKV + s * (kKTile + kVTile);
+      if (!TSK_IN_BOUNDS(p, cx.abort,
+                         w.g < p.Hkv && w.start_k + kt * kTileN < p.kv_rows &&
+                             (long long)(vt_tile0 + kt + 1) * 128 <= f.vt_cols,
+                         42)) {
+        ok = false;
+        break;
+      }
       mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kKTile);
       tma_load_3d(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, w.start_k + kt * kTileN);
       mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kVTile);
@@ -278,7 +305,8 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
       diag0 = w.offset + w.q0;
       pos = diag0 + r;
       if (p.sinks) {
-        m_used = __ldg(p.sinks + w.h0 + t) * 1.4426950408889634f;
+        if (TSK_IN_BOUNDS(p, cx.abort, w.h0 + t < p.Hq, 44))
+          m_used = __ldg(p.sinks + w.h0 + t) * 1.4426950408889634f;
         l = 1.f;
       }
     }
@@ -401,7 +429,9 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
       ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
     const int row = e.y + r;
     const size_t orow = (size_t)(e.x + row) * p.Hq + h;
-    if (p.lse && row < e.w) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    // (rows past the sequence's end are neither stored nor checked)
+    const bool row_ok = row < e.w && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
+    if (p.lse && row_ok) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
     if (e.y + wq * 32 + 32 <= e.w) {
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
@@ -412,11 +442,12 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
                      ob[4 * c + 2], ob[4 * c + 3]);
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && TSK_IN_BOUNDS(p, cx.abort,
+                                     h < p.Hq && e.x + e.y + wq * 32 + 32 <= p.q_rows, 46)) {
         tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, e.x + e.y + wq * 32);
         bulk_commit_group();
       }
-    } else if (row < e.w) {
+    } else if (row_ok) {
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * 64);
 #pragma unroll
       for (int c = 0; c < 8; ++c)

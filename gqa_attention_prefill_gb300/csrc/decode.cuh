@@ -50,6 +50,7 @@ struct DecParams {
   float scale_log2;         // scale * log2(e)
   unsigned long long timeout_ns;
   PagedKV kv;               // paged key/value cache, or kv.page_size == 0 (contiguous)
+  int kv_rows = 0;          // rows of the k/v buffers (checked by builds with -DTSK_DEBUG)
 };
 
 template <int D>
@@ -166,16 +167,25 @@ __global__ void __launch_bounds__(kThreads)
     const int s = i % kStages;
     if (i >= kStages) ok = ok && mbar_wait(bar_empty + 8 * s, ((i / kStages) - 1) & 1, 30, pw, abort_addr);
     if (!ok) return;
-    issued = i + 1;
     const int pos0 = lo_al + (t_begin + i) * kKeys;
+    if (!TSK_IN_BOUNDS(pw, abort_addr,
+                       g < p.Hkv && (p.kv.page_size != 0 ||
+                                     (k0 + pos0 >= 0 && k0 + pos0 < p.kv_rows)),
+                       51)) {
+      ok = false;
+      return;
+    }
+    issued = i + 1;
     const uint32_t dst = sbase + (uint32_t)s * 2u * kTile;
     mbar_arrive_expect_tx(bar_full + 8 * s, 2 * kTile);
+    bool in = true;
     for (int hf = 0; hf < D / 64; ++hf) {
-      tma_load_key_rows(dst + hf * (kKeys * 128), &tmK, bar_full + 8 * s, 64 * hf, g, p.kv, b, k0,
-                        pos0, Lk);
-      tma_load_key_rows(dst + kTile + hf * (kKeys * 128), &tmV, bar_full + 8 * s, 64 * hf, g, p.kv,
-                        b, k0, pos0, Lk);
+      in = tma_load_key_rows(dst + hf * (kKeys * 128), &tmK, bar_full + 8 * s, 64 * hf, g, p.kv, b,
+                             k0, pos0, Lk) && in;
+      in = tma_load_key_rows(dst + kTile + hf * (kKeys * 128), &tmV, bar_full + 8 * s, 64 * hf, g,
+                             p.kv, b, k0, pos0, Lk) && in;
     }
+    if (!TSK_IN_BOUNDS(pw, abort_addr, in, 43)) ok = false;
   };
   if (threadIdx.x == 0)
     for (int i = 0; i < kStages - 1 && i < nt; ++i) issue(i);
@@ -185,10 +195,12 @@ __global__ void __launch_bounds__(kThreads)
   {
     const int r0 = lane >> 2, r1 = r0 + 8, c = (lane & 3) * 2;
     const __nv_bfloat16* qb = p.q + ((size_t)b * p.Hq + (size_t)g * p.G + h_lo) * D;
+    const bool q_ok =
+        TSK_IN_BOUNDS(pw, abort_addr, b < p.num_seqs && g * p.G + h_lo + rows <= p.Hq, 52);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       auto ld = [&](int r, int col) -> uint32_t {
-        return r < rows ? *reinterpret_cast<const uint32_t*>(qb + (size_t)r * D + col) : 0u;
+        return r < rows && q_ok ? *reinterpret_cast<const uint32_t*>(qb + (size_t)r * D + col) : 0u;
       };
       qa[ks][0] = ld(r0, 16 * ks + c);
       qa[ks][1] = ld(r1, 16 * ks + c);
@@ -331,7 +343,8 @@ __global__ void __launch_bounds__(kThreads)
       wt[w] = mw[w] == -INFINITY ? 0.f : ex2_approx(mw[w] - M);
       L += wt[w] * red[((size_t)w * kRows + r) * (D + 2) + D + 1];
     }
-    if (r < rows) {
+    if (r < rows && TSK_IN_BOUNDS(pw, abort_addr,
+                                  split < p.splits && g * p.G + h_lo + r < p.Hq, 53)) {
       const int h = g * p.G + h_lo + r;
       float* dst = p.part + (((size_t)split * p.num_seqs + b) * p.Hq + h) * (D + 2);
 #pragma unroll
@@ -356,7 +369,9 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const int prev = atomicAdd(p.counters + ((size_t)b * p.Hkv + g) * p.n_hb + hb, 1);
+    int prev = 0;
+    if (TSK_IN_BOUNDS(pw, abort_addr, b < p.num_seqs && g < p.Hkv && hb < p.n_hb, 54))
+      prev = atomicAdd(p.counters + ((size_t)b * p.Hkv + g) * p.n_hb + hb, 1);
     s_last = prev == p.splits - 1;
     if (s_last) __threadfence();
   }
@@ -366,7 +381,7 @@ __global__ void __launch_bounds__(kThreads)
     // 128 threads: eight per query head of the block, D / 8 columns each.
     const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
     constexpr int per = D / 8;
-    if (r < rows) {
+    if (r < rows && TSK_IN_BOUNDS(pw, abort_addr, g * p.G + h_lo + r < p.Hq, 55)) {
       const int h = g * p.G + h_lo + r;
       const float sink2 = p.sinks ? p.sinks[h] * 1.4426950408889634f : -INFINITY;
       auto src_of = [&](int sp) {

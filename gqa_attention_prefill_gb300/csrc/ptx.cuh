@@ -181,6 +181,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int sit
 #endif
 }
 
+// ----------------------------------------------------------------- bounds
+// Builds with -DTSK_DEBUG check every computed global index and TMA
+// coordinate against the extent of its buffer before the access
+// (TSK_IN_BOUNDS(p, abort, condition, site)).  A failed check records
+// TSK_ERR_BOUNDS (-9), the site and the block in p.status[0..2] (first error
+// wins), raises the CTA's abort flag so that the other roles' bounded waits
+// give up, and the caller skips the access.  The kernel never traps.  In other
+// builds the check is `true` and costs nothing.
+#ifdef TSK_DEBUG
+template <class P>
+__device__ __noinline__ bool bounds_fail(const P& p, uint32_t abort_saddr, int site) {
+  if (atomicCAS(p.status, 0, -9) == 0) {
+    p.status[1] = site;
+    p.status[2] = (int)blockIdx.x;
+  }
+  if (abort_saddr) st_shared_volatile(abort_saddr, 1);
+  return false;
+}
+#define TSK_IN_BOUNDS(p, abort, cond, site) ((cond) || ::tsk::bounds_fail((p), (abort), (site)))
+#else
+#define TSK_IN_BOUNDS(p, abort, cond, site) true
+#endif
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -192,37 +215,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-
-// L2 eviction policies for TMA copies: data read once (evict first) and data
-// read again by other CTAs later (evict last).
-__device__ __forceinline__ uint64_t l2_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-// tma_load_3d with an L2 eviction policy.
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                 int c0, int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
-      : "memory");
-}
-// tma_store_3d with an L2 eviction policy.
-__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, uint32_t src, int c0,
-                                                  int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
-      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(m)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
 }
 
@@ -380,6 +372,12 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 

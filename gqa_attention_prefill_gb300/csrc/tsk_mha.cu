@@ -67,6 +67,7 @@ bool g_ev_recorded = false;
 
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits give up after 2 s
 int g_debug_stall = 0;
+int g_debug_shrink = 0;  // debug builds: rows taken off the checked extent of q/out
 
 thread_local char g_last_error[256] = "";
 
@@ -235,6 +236,7 @@ const char* tsk_status_string(tsk_status s) {
     case TSK_ERR_LAUNCH: return "kernel launch failed";
     case TSK_ERR_DEVICE_TIMEOUT: return "device-side bounded wait expired";
     case TSK_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with total_tokens";
+    case TSK_ERR_BOUNDS: return "index or TMA coordinate out of bounds (debug build; access skipped)";
   }
   return "unknown status";
 }
@@ -476,6 +478,12 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = g_debug_stall;
   p.kv = pg;
+  p.q_rows = (int)total_q;
+#ifdef TSK_DEBUG
+  p.q_rows -= g_debug_shrink;
+#endif
+  p.kv_rows = (int)kv_rows;
+  p.max_tiles = ws->max_tiles;
   p.knorm = knorm_ext ? knorm_ext
                       : norm_blocks ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
@@ -541,6 +549,8 @@ tsk_status tsk_get_device_status(tsk_stream_t stream_) {
   if (cudaMemcpy(hdr, it->second.base, sizeof hdr, cudaMemcpyDeviceToHost) != cudaSuccess)
     return cuda_fail(cudaErrorUnknown);
   if (hdr[0] != 0) {
+    snprintf(g_last_error, sizeof g_last_error, "device status %d at site %d, block %d", hdr[0],
+             hdr[1], hdr[2]);
     int zero[4] = {0, 0, 0, 0};
     cudaMemcpy(it->second.base, zero, sizeof zero, cudaMemcpyHostToDevice);
   }
@@ -597,6 +607,20 @@ tsk_status tsk_release(void) {
   if (dev >= 0) cudaSetDevice(dev);
   g_ws.clear();
   return TSK_OK;
+}
+
+// Test hook of builds with -DTSK_DEBUG: checks of later prefill calls use a
+// q/out extent `rows` smaller than the real one.
+tsk_status tsk_debug_shrink_extent(int32_t rows) {
+#ifdef TSK_DEBUG
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (rows < 0) return TSK_ERR_INVALID_ARG;
+  g_debug_shrink = rows;
+  return TSK_OK;
+#else
+  (void)rows;
+  return TSK_ERR_UNSUPPORTED;
+#endif
 }
 
 // Test hook: wait limit for later calls (0 = default 2 s) and stall injection.
@@ -724,6 +748,9 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = 0;
   p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
+  p.q_rows = (int)total_tokens;
+  p.kv_rows = (int)total_tokens;
+  p.max_tiles = kNoAllocMaxTiles;
   p.knorm = norm_blocks ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
@@ -877,6 +904,7 @@ tsk_status decode_impl(const void* q, const void* k, const void* v, const float*
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.kv = pg;
+  p.kv_rows = (int)kv_rows;
 
   char name[160];
   snprintf(name, sizeof name, "%s[Hq=%d,Hkv=%d,D=%d,W=%d,nseq=%d,Tk=%lld,splits=%d]", what, Hq,
@@ -1068,7 +1096,12 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   p.timeout_ns = g_timeout_ns;
   p.debug_stall = g_debug_stall;
   p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
+  p.q_rows = (int)total_tokens;
+  p.kv_rows = (int)total_tokens;
+  p.max_tiles = ws->max_tiles;
   f.tile_off = tile_off;
+  f.num_seqs = num_seqs;
+  f.vt_cols = t_pad;
   f.v_scale = v_scale;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);

@@ -47,7 +47,9 @@ typedef enum {
   TSK_ERR_OOM = -5,            /* workspace allocation failed */
   TSK_ERR_LAUNCH = -6,         /* kernel launch failed */
   TSK_ERR_DEVICE_TIMEOUT = -7, /* a kernel gave up on a bounded wait (device status word) */
-  TSK_ERR_BAD_SEQLENS = -8     /* device check: cu_seqlens not 0..total_tokens non-decreasing */
+  TSK_ERR_BAD_SEQLENS = -8,    /* device check: cu_seqlens not 0..total_tokens non-decreasing */
+  TSK_ERR_BOUNDS = -9          /* libraries built with -DTSK_DEBUG only: a computed global index or
+                                  TMA coordinate fell outside its buffer; the access was skipped */
 } tsk_status;
 
 /*
@@ -272,6 +274,16 @@ TSK_API tsk_status tsk_debug_set_wait(unsigned long long timeout_ns, int stall);
  * launch.
  */
 TSK_API tsk_status tsk_debug_trace(unsigned long long *out, int32_t n);
+
+/*
+ * tsk_debug_shrink_extent -- test hook of libraries built with -DTSK_DEBUG
+ * (otherwise TSK_ERR_UNSUPPORTED): later prefill calls check their q/out
+ * accesses against an extent `rows` smaller than the real one (the tensor
+ * maps keep the real extent, so every access it makes the checks skip is a
+ * legal one).  The checks then report TSK_ERR_BOUNDS and leave the last
+ * rows unwritten; 0 restores the real extent.
+ */
+TSK_API tsk_status tsk_debug_shrink_extent(int32_t rows);
 
 /*
  * tsk_debug_timeline -- libraries built with -DTSK_TIMELINE only (otherwise

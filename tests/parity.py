@@ -48,7 +48,7 @@ def run_gpu(w: inputgen.Workload, d=None, with_lse=True, check_status=True):
     torch.cuda.synchronize()
     if check_status:
         st = pkg.tsk_get_device_status()
-        assert st == 0, pkg.STATUS.get(st, st)
+        assert st == 0, f"{pkg.STATUS.get(st, st)}: {pkg.tsk_last_error()}"
     return out, lse
 
 

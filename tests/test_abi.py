@@ -182,3 +182,12 @@ def test_host_buffer_entry_rejects_out_overlapping_inputs(lib):
     rc = pkg.tsk_mha_prefill_host(q, kv, kv, None, cu, 1, T, Hq, Hkv, D, 0, 0.125,
                                   q.ctypes.data + 128, None, 0)
     assert rc == -1
+
+
+def test_bounds_checked_build_compiles_and_exports_the_same_symbols(tmp_path):
+    from gqa_attention_prefill_gb300 import build
+    path = build.build(out=str(tmp_path / "libtsk_mha_debug.so"), defines=["TSK_DEBUG"])
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                         text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == set(declared_functions())
