@@ -763,18 +763,31 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
   uint32_t s_cnt = 0, pv_cnt = 0;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
+  // The next unit and its sink are loaded before a unit's epilogue, so that
+  // their latency passes while the epilogue waits for the last PV.
+  auto fetch = [&](int uu, Unit& w, float& sink) {
+    if (uu >= cx.total_units) return;
+    w = decode_unit<QS>(p, uu);
+    const int h = tile_head<QS>(w, t);
+    sink = -INFINITY;
+    if (t < w.ntiles && p.sinks && TSK_IN_BOUNDS(p, cx.abort, h >= 0 && h < p.Hq, 44))
+      sink = __ldg(p.sinks + h) * 1.4426950408889634f;
+  };
+  Unit wn;
+  float sink_n = -INFINITY;
+  fetch(blockIdx.x, wn, sink_n);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit<QS>(p, u);
-    if (t >= w.ntiles) continue;
+    const Unit w = wn;
+    const float sink = sink_n;
+    if (t >= w.ntiles) {
+      fetch(u + gridDim.x, wn, sink_n);
+      continue;
+    }
     const int h = tile_head<QS>(w, t);
     const int q0t = tile_q0<QS>(w, t);  // first query row of this tile
     const int row = q0t + r;           // query row, relative to the sequence's first query
     const int pos = w.offset + row;    // its key position
-    float m_used = -INFINITY, l = 0.f;
-    if (p.sinks && TSK_IN_BOUNDS(p, cx.abort, h >= 0 && h < p.Hq, 44)) {
-      m_used = __ldg(p.sinks + h) * 1.4426950408889634f;
-      l = 1.f;
-    }
+    float m_used = sink, l = sink == -INFINITY ? 0.f : 1.f;
     for (int j = 0; j < w.n_kv; ++j) {
       const int kt = w.kv_lo + j;
       ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort);
@@ -914,6 +927,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
     }
     if (!ok) break;
+    fetch(u + gridDim.x, wn, sink_n);
     // ------------------------------------------------------------ epilogue
     TSK_TRACE_T0(tr_epi);
     ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
@@ -926,14 +940,19 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     tmem_wait_ld();
     reg_fence<64>(o);
     const float inv = rcp_approx(l);
+    const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t ob[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
-      ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+    for (int c = 0; c < 32; ++c) {
+      float a, b;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1])), inv2),
+                a, b);
+      ob[c] = pack_bf16x2(a, b);
+    }
     const size_t orow = (size_t)(w.start + row) * p.Hq + h;
     // (rows past the sequence's end are neither stored nor checked)
     const bool row_ok = row < w.len && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
-    if (p.lse && row_ok) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    if (p.lse && row_ok) p.lse[orow] = (m_used + lg2_approx(l)) * 0.69314718055994531f;
     if (q0t + wq * 32 + 32 <= w.len) {
       // The warp's 32 rows lie inside the sequence: stage them in this warp's
       // slice of the staging tile and store them with one TMA bulk store.

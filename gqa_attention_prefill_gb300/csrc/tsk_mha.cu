@@ -67,7 +67,9 @@ bool g_ev_recorded = false;
 
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits give up after 2 s
 int g_debug_stall = 0;
-int g_debug_shrink = 0;  // debug builds: rows taken off the checked extent of q/out
+#ifdef TSK_DEBUG
+int g_debug_shrink = 0;  // rows taken off the checked extent of q/out
+#endif
 
 thread_local char g_last_error[256] = "";
 
@@ -346,7 +348,9 @@ void launch_attention(int D, int window, int qstep, int grid, const CUtensorMap&
 // The key-norm pre-pass (extra scheduler blocks) for a D = 64 prefill: the
 // kernel bounds every score of a row by its query norm times the largest
 // key norm of the KV head and skips the row maximum while that bound allows
-// it.  Returns the number of extra blocks (0: no bound; too many KV heads).
+// it (the D = 128 kernel keeps computing it: there the extra state of the
+// bound spilled registers and cost 18-23%).  Returns the number of extra
+// blocks (0: no bound; too many KV heads).
 int key_norm_setup(tsk::KeyNorms* kn, const void* k, int64_t rows, int Hkv, int D, float* out) {
   *kn = tsk::KeyNorms{nullptr, 0, 0, 0, nullptr};
   if (D != 64 || Hkv > tsk::kNormMaxHeads || rows <= 0) return 0;
