@@ -530,10 +530,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       tc_fence_after();
       TSK_TRACE_T0(tr_ld);
       uint32_t sr[128];
-      tmem_ld_32x32b_x32(tS + 0, sr + 0);
-      tmem_ld_32x32b_x32(tS + 32, sr + 32);
-      tmem_ld_32x32b_x32(tS + 64, sr + 64);
-      tmem_ld_32x32b_x32(tS + 96, sr + 96);
+      tmem_ld_32x32b_x128(tS, sr);  // (one 128-column load: fewer instructions than four)
       tmem_wait_ld();
       reg_fence<128>(sr);
       TSK_TRACE_ADD(20, tr_ld);
@@ -632,20 +629,17 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
         {
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
             uint32_t o[64];
-            tmem_ld_32x32b_x32(tO, o);
-            tmem_ld_32x32b_x32(tO + 32, o + 32);
+            tmem_ld_32x32b_x64(tO, o);
             tmem_wait_ld();
             reg_fence<64>(o);
 #pragma unroll
             for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st_32x32b_x32(tO, o);
-            tmem_st_32x32b_x32(tO + 32, o + 32);
+            tmem_st_32x32b_x64(tO, o);
           }
         }
       }
       TSK_TRACE_T0(tr_st);
-      tmem_st_32x32b_x32(tP, pk);
-      tmem_st_32x32b_x32(tP + 32, pk + 32);
+      tmem_st_32x32b_x64(tP, pk);
       tmem_wait_st();
       TSK_TRACE_ADD(23, tr_st);
       tc_fence_before();
@@ -684,8 +678,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     ++pv_cnt;
     tc_fence_after();
     uint32_t o[64];
-    tmem_ld_32x32b_x32(tO, o);
-    tmem_ld_32x32b_x32(tO + 32, o + 32);
+    tmem_ld_32x32b_x64(tO, o);
     tmem_wait_ld();
     reg_fence<64>(o);
     TSK_EV(12);
@@ -810,8 +803,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       for (int hf = 0; hf < 2; ++hf) {
         TSK_TRACE_T0(tr_ld);
         uint32_t sr[64];
-        tmem_ld_32x32b_x32(tS + 64 * hf, sr);
-        tmem_ld_32x32b_x32(tS + 64 * hf + 32, sr + 32);
+        tmem_ld_32x32b_x64(tS + 64 * hf, sr);
         tmem_wait_ld();
         reg_fence<64>(sr);
         TSK_TRACE_ADD(20, tr_ld);
@@ -918,8 +910,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
         }
       }
       TSK_TRACE_T0(tr_st);
-      tmem_st_32x32b_x32(tP, pk);
-      tmem_st_32x32b_x32(tP + 32, pk + 32);
+      tmem_st_32x32b_x64(tP, pk);
       tmem_wait_st();
       TSK_TRACE_ADD(23, tr_st);
       tc_fence_before();
@@ -935,8 +926,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     ++pv_cnt;
     tc_fence_after();
     uint32_t o[64];
-    tmem_ld_32x32b_x32(tO, o);
-    tmem_ld_32x32b_x32(tO + 32, o + 32);
+    tmem_ld_32x32b_x64(tO, o);
     tmem_wait_ld();
     reg_fence<64>(o);
     const float inv = rcp_approx(l);

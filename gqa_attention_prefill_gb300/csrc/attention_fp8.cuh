@@ -317,10 +317,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
       ++s_cnt;
       tc_fence_after();
       uint32_t sr[128];
-      tmem_ld_32x32b_x32(tS + 0, sr + 0);
-      tmem_ld_32x32b_x32(tS + 32, sr + 32);
-      tmem_ld_32x32b_x32(tS + 64, sr + 64);
-      tmem_ld_32x32b_x32(tS + 96, sr + 96);
+      tmem_ld_32x32b_x128(tS, sr);
       tmem_wait_ld();
       reg_fence<128>(sr);
       tc_fence_before();
@@ -390,14 +387,12 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t o[64];
-          tmem_ld_32x32b_x32(tO, o);
-          tmem_ld_32x32b_x32(tO + 32, o + 32);
+          tmem_ld_32x32b_x64(tO, o);
           tmem_wait_ld();
           reg_fence<64>(o);
 #pragma unroll
           for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st_32x32b_x32(tO, o);
-          tmem_st_32x32b_x32(tO + 32, o + 32);
+          tmem_st_32x32b_x64(tO, o);
         }
       }
       tmem_st_32x32b_x32(tP, pk);
@@ -418,20 +413,24 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
     ++pv_cnt;
     tc_fence_after();
     uint32_t o[64];
-    tmem_ld_32x32b_x32(tO, o);
-    tmem_ld_32x32b_x32(tO + 32, o + 32);
+    tmem_ld_32x32b_x64(tO, o);
     tmem_wait_ld();
     reg_fence<64>(o);
     const float inv = f.v_scale * rcp_approx(l);
     uint32_t ob[32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
-      ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+    for (int c = 0; c < 32; ++c) {
+      float a, b;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1])),
+                       f2_pack(inv, inv)),
+                a, b);
+      ob[c] = pack_bf16x2(a, b);
+    }
     const int row = e.y + r;
     const size_t orow = (size_t)(e.x + row) * p.Hq + h;
     // (rows past the sequence's end are neither stored nor checked)
     const bool row_ok = row < e.w && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
-    if (p.lse && row_ok) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
+    if (p.lse && row_ok) p.lse[orow] = (m_used + lg2_approx(l)) * 0.69314718055994531f;
     if (e.y + wq * 32 + 32 <= e.w) {
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
