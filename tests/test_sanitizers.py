@@ -62,5 +62,7 @@ def test_library_host_side(tmp_path):
     # (nvcc splits -Xcompiler arguments at commas: one sanitizer per flag)
     lib = build.build(out=str(tmp_path / "libtsk_mha_san.so"),
                       host_flags=["-fsanitize=address", "-fsanitize=undefined", *SAN[1:]])
-    out = _run_sanitized({"TSK_LIB_PATH": lib}, ["tests/test_abi.py", "-m", "not gpu"])
+    # (the test that compiles another build runs the compiler: not under the ASan runtime)
+    out = _run_sanitized({"TSK_LIB_PATH": lib}, ["tests/test_abi.py", "-m", "not gpu",
+                                                 "-k", "not bounds_checked_build"])
     assert "passed" in out
