@@ -601,22 +601,26 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
       TSK_TRACE_T0(tr_exp);
       // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per element,
-      // four scalar partial sums, bf16x2 packing for TMEM.
+      // packed partial sums, bf16x2 packing for TMEM.
       uint32_t pk[64];
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm = f2_pack(-m_use, -m_use);
       {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // (row sums in two packed f32x2 accumulators: one add per pair)
+        uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm), x0, x1);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
-          acc[c & 3] += p0 + p1;
+          acc2[c & 1] = f2_add(acc2[c & 1], f2_pack(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
-        l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        float a0, a1, b0, b1;
+        f2_unpack(acc2[0], a0, a1);
+        f2_unpack(acc2[1], b0, b1);
+        l += (a0 + b0) + (a1 + b1);
       }
       TSK_TRACE_ADD(22, tr_exp);
       TSK_EV(5);
@@ -868,7 +872,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
         }
         const float m_use = m_used == -INFINITY ? 0.f : m_used;
         // p = 2^(s*scale*log2e - m): packed FMA on column pairs, exp2 per
-        // element, four scalar partial sums, bf16x2 packing.
+        // element, packed partial sums, bf16x2 packing.
         TSK_TRACE_T0(tr_exp);
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint64_t negm[2];  // -m, or -inf for chunks hidden from the whole warp
@@ -877,17 +881,20 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
           const float nm = (cm.none & (1u << (2 * hf + kk))) ? -INFINITY : -m_use;
           negm[kk] = f2_pack(nm, nm);
         }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sl2x2, negm[c >> 4]), x0, x1);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
-          acc[c & 3] += p0 + p1;
+          acc2[c & 1] = f2_add(acc2[c & 1], f2_pack(p0, p1));
           pk[32 * hf + c] = pack_bf16x2(p0, p1);
         }
-        l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        float a0, a1, b0, b1;
+        f2_unpack(acc2[0], a0, a1);
+        f2_unpack(acc2[1], b0, b1);
+        l += (a0 + b0) + (a1 + b1);
         TSK_TRACE_ADD(22, tr_exp);
       }
       if (j > 0) {

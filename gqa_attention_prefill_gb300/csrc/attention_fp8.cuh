@@ -368,7 +368,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
       uint32_t pk[32];
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm = f2_pack(-m_use, -m_use);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t acc2[2] = {0ull, 0ull};  // packed partial sums: one add per pair
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         float x0, x1, x2, x3;
@@ -376,10 +376,16 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
         f2_unpack(f2_fma(f2_pack(s[4 * c + 2], s[4 * c + 3]), sl2x2, negm), x2, x3);
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        acc[c & 3] += (p0 + p1) + (p2 + p3);
+        acc2[0] = f2_add(acc2[0], f2_pack(p0, p1));
+        acc2[1] = f2_add(acc2[1], f2_pack(p2, p3));
         pk[c] = pack_e4m3x4(p0, p1, p2, p3);
       }
-      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(acc2[0], a0, a1);
+        f2_unpack(acc2[1], b0, b1);
+        l += (a0 + b0) + (a1 + b1);
+      }
       if (j > 0) {
         ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
         if (!ok) break;
