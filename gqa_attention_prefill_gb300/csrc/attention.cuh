@@ -1031,6 +1031,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // Everything above overlaps the scheduler's tail; its outputs (the unit
+  // list, the tile count, the key norms) are read only after this.
+  griddep_wait();
   if (warp == 3 && p.knorm)
     for (int g = lane; g < p.Hkv; g += 32) st_shared_f32(cx.sbase + kSmemNorm + 4u * g, __ldg(p.knorm + g));
   trace_init();

@@ -83,6 +83,19 @@ __device__ __forceinline__ void trace_cta_start() {}
 __device__ __forceinline__ void trace_cta_time() {}
 #endif
 
+// ----------------------------------------------------------------- launch order
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel of its stream is still
+// running; griddep_wait() returns once that kernel has completed and its
+// memory writes are visible (immediately for a kernel launched without the
+// attribute).  griddep_launch_dependents() lets the next kernel start early.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -30,7 +30,7 @@ constexpr int kWsHeader = 8;   // ints; tile offsets follow, then the int4 list 
 // bounds every score of a query row q by ||q|| * max||k||.  Run for at most
 // kNormMaxHeads KV heads by at most kNormBlocks blocks; its buffer holds
 // kNormBlocks * kNormMaxHeads per-block maxima, then kNormMaxHeads results.
-constexpr int kNormBlocks = 32;
+constexpr int kNormBlocks = 148;
 constexpr int kNormMaxHeads = 256;
 constexpr int kNormFloats = (kNormBlocks + 1) * kNormMaxHeads;
 
@@ -83,31 +83,49 @@ __device__ __forceinline__ bool pages_ok(const PagedKV& pg, int s, int Lk) {
 
 // Blocks 1.. of the scheduler launch: per-head maxima of key-row norms over
 // a grid-stride share of the rows; the last block to finish reduces the
-// per-block maxima and resets the counter.  Norms are non-negative, so their
-// bit patterns order like the values (shared-memory integer maxima); a NaN
-// norm orders above every finite one and disables the bound for its head.
+// per-block maxima and resets the counter.  Eight consecutive threads read
+// the eight 16-byte chunks of one key row (D = 64), so a warp reads four
+// whole rows, 512 contiguous bytes, per load; the eight partial sums of a row
+// are combined with shuffles (a fixed order: the result does not depend on
+// the number of blocks).  Norms are non-negative, so their bit patterns order
+// like the values (shared-memory integer maxima); a NaN norm orders above
+// every finite one and disables the bound for its head.
 __device__ void key_norm_blocks(const KeyNorms& kn, int* __restrict__ ws, int* s_max,
                                 int* s_last, int blk, int nblk) {
   const int tid = threadIdx.x;
   for (int g = tid; g < kn.heads; g += kSchedThreads) s_max[g] = 0;
   __syncthreads();
-  const long long total = kn.rows * kn.heads;
-  const int chunks = kn.D / 8;  // 16-byte chunks of a row
-  for (long long r = (long long)blk * kSchedThreads + tid; r < total;
-       r += (long long)nblk * kSchedThreads) {
-    const uint4* row = kn.k + r * chunks;
-    float acc = 0.f;
-    for (int c = 0; c < chunks; ++c) {
-      const uint4 v = __ldg(row + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // 16-byte chunks in all (8 per row); the stride keeps tid % 8 = chunk % 8, so
+  // the eight threads of a row stay together in the loop.
+  const long long total = kn.rows * kn.heads * 8;
+  const long long stride = (long long)nblk * kSchedThreads;
+  const unsigned group = 0xFFu << (tid & 24);  // the 8 lanes sharing this thread's row
+  // kUnroll loads in flight per thread (enough bytes in flight to stream HBM)
+  constexpr int kUnroll = 4;
+  for (long long i0 = (long long)blk * kSchedThreads + tid; i0 < total; i0 += kUnroll * stride) {
+    uint4 v[kUnroll];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      v[u] = i < total ? __ldg(kn.k + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i >= total) break;  // (the same for the 8 lanes of a row)
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
         acc = fmaf(lo, lo, acc);
         acc = fmaf(hi, hi, acc);
       }
+      acc += __shfl_xor_sync(group, acc, 1);
+      acc += __shfl_xor_sync(group, acc, 2);
+      acc += __shfl_xor_sync(group, acc, 4);
+      if ((tid & 7) == 0) atomicMax(&s_max[(int)((i >> 3) % kn.heads)], __float_as_int(sqrtf(acc)));
     }
-    atomicMax(&s_max[(int)(r % kn.heads)], __float_as_int(sqrtf(acc)));
   }
   __syncthreads();
   for (int g = tid; g < kn.heads; g += kSchedThreads)
@@ -117,13 +135,17 @@ __device__ void key_norm_blocks(const KeyNorms& kn, int* __restrict__ ws, int* s
   if (tid == 0) *s_last = atomicAdd(&ws[kWsNormCount], 1) == nblk - 1;
   __syncthreads();
   if (*s_last) {
+    // every (block, head) maximum read by its own thread, reduced in shared memory
     __threadfence();
-    for (int g = tid; g < kn.heads; g += kSchedThreads) {
-      int m = 0;
-      for (int b = 0; b < nblk; ++b)
-        m = max(m, __float_as_int(__ldcg(kn.out + b * kNormMaxHeads + g)));
-      kn.out[kNormBlocks * kNormMaxHeads + g] = __int_as_float(m);
+    for (int g = tid; g < kn.heads; g += kSchedThreads) s_max[g] = 0;
+    __syncthreads();
+    for (int i = tid; i < nblk * kn.heads; i += kSchedThreads) {
+      const int b = i / kn.heads, g = i - b * kn.heads;
+      atomicMax(&s_max[g], __float_as_int(__ldcg(kn.out + b * kNormMaxHeads + g)));
     }
+    __syncthreads();
+    for (int g = tid; g < kn.heads; g += kSchedThreads)
+      kn.out[kNormBlocks * kNormMaxHeads + g] = __int_as_float(s_max[g]);
     if (tid == 0) ws[kWsNormCount] = 0;
   }
 }
@@ -146,6 +168,9 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   __shared__ int s_cursor[kCostBins];
   __shared__ int s_bad, s_base;
   const int tid = threadIdx.x;
+  // The attention kernel may be launched now: it waits for this grid's
+  // completion before it reads anything this grid writes.
+  griddep_launch_dependents();
   if (blockIdx.x > 0) {
     key_norm_blocks(kn, ws, s_hist, &s_bad, blockIdx.x - 1, gridDim.x - 1);
     return;

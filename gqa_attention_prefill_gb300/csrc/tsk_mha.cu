@@ -324,19 +324,33 @@ namespace {
 // The attention kernel for head dimension D (64 or 128), the window and the
 // unit layout (qstep: 0 = two heads of a group over the same rows, kTileM =
 // two row blocks of one head).
+// The D = 64 kernels follow the scheduler on the stream with programmatic
+// stream serialisation: their CTAs may start (barrier set-up, TMEM
+// allocation) while the scheduler finishes, and wait for its results on the
+// device.
 template <int QS>
 void launch_attention_qs(int D, int window, int grid, const CUtensorMap& tq,
                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                          const tsk::AttnParams& p, cudaStream_t stream) {
-  if (D == 128)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(tsk::kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (D == 128) {  // (an ordinary launch: 1.3% faster here than with the attribute)
     tsk::d128::attention_fwd_d128_kernel<QS>
         <<<grid, tsk::kThreads, tsk::d128::kSmemBytes, stream>>>(tq, tk, tv, to, p);
-  else if (window > 0 && window <= tsk::kSmallWindowMax)
-    tsk::attention_fwd_kernel<true, QS>
-        <<<grid, tsk::kThreads, tsk::kSmemBytesWindow, stream>>>(tq, tk, tv, to, p);
-  else
-    tsk::attention_fwd_kernel<false, QS>
-        <<<grid, tsk::kThreads, tsk::kSmemBytesCausal, stream>>>(tq, tk, tv, to, p);
+  } else if (window > 0 && window <= tsk::kSmallWindowMax) {
+    cfg.dynamicSmemBytes = tsk::kSmemBytesWindow;
+    cudaLaunchKernelEx(&cfg, tsk::attention_fwd_kernel<true, QS>, tq, tk, tv, to, p);
+  } else {
+    cfg.dynamicSmemBytes = tsk::kSmemBytesCausal;
+    cudaLaunchKernelEx(&cfg, tsk::attention_fwd_kernel<false, QS>, tq, tk, tv, to, p);
+  }
 }
 void launch_attention(int D, int window, int qstep, int grid, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
@@ -355,7 +369,8 @@ int key_norm_setup(tsk::KeyNorms* kn, const void* k, int64_t rows, int Hkv, int 
   *kn = tsk::KeyNorms{nullptr, 0, 0, 0, nullptr};
   if (D != 64 || Hkv > tsk::kNormMaxHeads || rows <= 0) return 0;
   *kn = tsk::KeyNorms{reinterpret_cast<const uint4*>(k), (long long)rows, Hkv, D, out};
-  const int64_t want = (rows * Hkv + 8 * tsk::kSchedThreads - 1) / (8 * tsk::kSchedThreads);
+  // about four 16-byte chunks per thread, at most kNormBlocks blocks
+  const int64_t want = (rows * Hkv * 8 + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads);
   return (int)(want < tsk::kNormBlocks ? (want < 1 ? 1 : want) : tsk::kNormBlocks);
 }
 
@@ -657,7 +672,7 @@ constexpr size_t kNoAllocOffInts =
     ((size_t)tsk::kWsHeader + (size_t)kNoAllocMaxSeqs + 1 + 3) & ~(size_t)3;
 constexpr size_t kNoAllocBytes = kNoAllocOffInts * 4 +
                                  (size_t)kNoAllocMaxTiles * 4 * tsk::kTileEntryInts +
-                                 tsk::kNormFloats * 4;  // ~1.6 MB
+                                 tsk::kNormFloats * 4;  // ~1.8 MB
 
 static __device__ __align__(256) int g_noalloc_scratch[kNoAllocBytes / 4];
 

@@ -304,8 +304,9 @@ TSK_API tsk_status tsk_debug_timeline(unsigned long long *out, int32_t n);
  * entry point; it is an addition of this library.)
  *
  * It calls no cudaMalloc/cudaFree or other allocating routine.  Its scratch
- * (status words, tile offsets, the sorted query-tile list) is a fixed
- * ~1.6 MB array in the library's device memory, which every GPU that loads
+ * (status words, tile offsets, the sorted query-tile list, the key-norm
+ * pre-pass's per-block maxima) is a fixed
+ * ~1.8 MB array in the library's device memory, which every GPU that loads
  * the library holds until the process exits.  Limits: num_seqs <= 16384 and
  * total_tokens/128 + num_seqs + 1 <= 49152; larger problems are rejected with
  * TSK_ERR_UNSUPPORTED (tsk_last_error says which limit) before anything is
