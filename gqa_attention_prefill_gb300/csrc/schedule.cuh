@@ -158,15 +158,48 @@ __global__ void __launch_bounds__(kSchedThreads, 1) key_norm_kernel(KeyNorms kn,
   key_norm_blocks(kn, ws, s_max, &s_last, blockIdx.x, gridDim.x);
 }
 
+// Exclusive prefix sum of v over the block (every thread calls it); *total
+// receives the block's sum.  Warp shuffles, then one warp over the 32 warp sums.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  static_assert(kSchedThreads == 1024, "32 warps");
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int r = (wid ? s_warp[wid - 1] : 0) + x - v;
+  *total = s_warp[31];
+  __syncthreads();  // (s_warp is reused by the next call)
+  return r;
+}
+
+// Sequences whose offsets the scheduler block keeps in shared memory; beyond
+// this it reads them (and the tile offsets) from global memory.
+constexpr int kSchedSmemSeqs = 2048;
+
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k,
                     int num_seqs, int total_tokens, int total_keys, int window,
                     int* __restrict__ ws, int* __restrict__ tile_off, int4* __restrict__ list,
                     int max_tiles, PagedKV pg, int entry_rows, KeyNorms kn) {
-  __shared__ int s_scan[kSchedThreads];
-  __shared__ int s_hist[kCostBins];
-  __shared__ int s_cursor[kCostBins];
-  __shared__ int s_bad, s_base;
+  __shared__ int s_hist[kCostBins];  // cost histogram, then the bins' write cursors
+  __shared__ int s_cu[kSchedSmemSeqs + 1], s_cuk[kSchedSmemSeqs + 1], s_off[kSchedSmemSeqs + 1];
+  __shared__ int s_warp[32];
+  __shared__ int s_bad;
   const int tid = threadIdx.x;
   // The attention kernel may be launched now: it waits for this grid's
   // completion before it reads anything this grid writes.
@@ -175,45 +208,52 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     key_norm_blocks(kn, ws, s_hist, &s_bad, blockIdx.x - 1, gridDim.x - 1);
     return;
   }
+  const bool small = num_seqs <= kSchedSmemSeqs;
   if (tid == 0) {
-    s_bad = (cu[0] != 0 || cu[num_seqs] != total_tokens || cu_k[0] != 0 ||
-             cu_k[num_seqs] != total_keys) ? 1 : 0;
-    s_base = 0;
+    const int c0 = cu[0], k0 = cu_k[0];
+    s_bad = (c0 != 0 || cu[num_seqs] != total_tokens || k0 != 0 || cu_k[num_seqs] != total_keys)
+                ? 1 : 0;
+    if (small) {
+      s_cu[0] = c0;
+      s_cuk[0] = k0;
+    }
   }
-  for (int i = tid; i < kCostBins; i += kSchedThreads) {
-    s_hist[i] = 0;
-    s_cursor[i] = 0;
-  }
-  __syncthreads();
+  for (int i = tid; i < kCostBins; i += kSchedThreads) s_hist[i] = 0;
+  __syncthreads();  // (s_bad is set before any thread can raise it)
 
   // Pass A: per-sequence tile counts -> exclusive prefix over sequences.
+  int base = 0;
   for (int c0 = 0; c0 < num_seqs; c0 += kSchedThreads) {
-    int s = c0 + tid;
+    const int s = c0 + tid;
     int nt = 0;
     if (s < num_seqs) {
-      int L = cu[s + 1] - cu[s];
-      const int Lk = cu_k[s + 1] - cu_k[s];
+      const int a = cu[s], b = cu[s + 1], ak = cu_k[s], bk = cu_k[s + 1];
+      if (small) {
+        s_cu[s + 1] = b;
+        s_cuk[s + 1] = bk;
+      }
+      int L = b - a;
+      const int Lk = bk - ak;
       if (L < 0 || Lk < L || !pages_ok(pg, s, Lk)) {
         s_bad = 1;
         L = 0;
       }
       nt = (L + entry_rows - 1) / entry_rows;
     }
-    s_scan[tid] = nt;
-    __syncthreads();
-    for (int off = 1; off < kSchedThreads; off <<= 1) {  // Hillis-Steele inclusive scan
-      int v = tid >= off ? s_scan[tid - off] : 0;
-      __syncthreads();
-      s_scan[tid] += v;
-      __syncthreads();
+    int chunk_total;
+    const int ex = block_exclusive_scan(nt, s_warp, &chunk_total);
+    if (s < num_seqs) {
+      tile_off[s] = base + ex;
+      if (small) s_off[s] = base + ex;
     }
-    if (s < num_seqs) tile_off[s] = s_base + s_scan[tid] - nt;
-    __syncthreads();
-    if (tid == kSchedThreads - 1) s_base += s_scan[tid];
-    __syncthreads();
+    base += chunk_total;
   }
-  const int n_tiles = s_base;
-  if (tid == 0) tile_off[num_seqs] = n_tiles;
+  const int n_tiles = base;
+  if (tid == 0) {
+    tile_off[num_seqs] = n_tiles;
+    if (small) s_off[num_seqs] = n_tiles;
+  }
+  __syncthreads();
   if (s_bad || n_tiles > max_tiles) {
     if (tid == 0) {
       ws[kWsNTiles] = 0;
@@ -221,28 +261,31 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     }
     return;
   }
-  __syncthreads();
 
-  // Pass B: cost histogram.  Tile i belongs to the last sequence whose offset <= i.
+  // Tile i belongs to the last sequence whose tile offset is <= i.
+  auto off_at = [&](int s) { return small ? s_off[s] : tile_off[s]; };
+  auto cu_at = [&](int s) { return small ? s_cu[s] : cu[s]; };
+  auto cuk_at = [&](int s) { return small ? s_cuk[s] : cu_k[s]; };
   auto seq_of = [&](int i) {
     int lo = 0, hi = num_seqs - 1;
     while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (tile_off[mid] <= i) lo = mid;
+      const int mid = (lo + hi + 1) >> 1;
+      if (off_at(mid) <= i) lo = mid;
       else hi = mid - 1;
     }
     return lo;
   };
+  // Pass B: cost histogram.
   for (int i = tid; i < n_tiles; i += kSchedThreads) {
-    int s = seq_of(i);
-    int qt = i - tile_off[s];
-    const int len = cu[s + 1] - cu[s];
+    const int s = seq_of(i);
+    const int qt = i - off_at(s);
+    const int len = cu_at(s + 1) - cu_at(s);
     const int cost =
-        qtile_key_range(qt * entry_rows, len, (cu_k[s + 1] - cu_k[s]) - len, window, entry_rows).y;
+        qtile_key_range(qt * entry_rows, len, (cuk_at(s + 1) - cuk_at(s)) - len, window, entry_rows).y;
     atomicAdd(&s_hist[min(cost, kCostBins) - 1], 1);
   }
   __syncthreads();
-  // Exclusive offsets in descending cost order: bin b starts after all bins > b.
+  // Write cursors in descending cost order: bin b starts after all bins > b.
   {
     constexpr int per = kCostBins / kSchedThreads;
     int local[per];
@@ -252,33 +295,26 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
       local[k] = s_hist[kCostBins - 1 - (tid * per + k)];
       sum += local[k];
     }
-    s_scan[tid] = sum;
-    __syncthreads();
-    for (int off = 1; off < kSchedThreads; off <<= 1) {
-      int v = tid >= off ? s_scan[tid - off] : 0;
-      __syncthreads();
-      s_scan[tid] += v;
-      __syncthreads();
-    }
-    int run = s_scan[tid] - sum;
+    int total;
+    int run = block_exclusive_scan(sum, s_warp, &total);  // (its barriers order the reads above)
 #pragma unroll
     for (int k = 0; k < per; ++k) {
-      s_cursor[kCostBins - 1 - (tid * per + k)] = run;
+      s_hist[kCostBins - 1 - (tid * per + k)] = run;
       run += local[k];
     }
   }
   __syncthreads();
   // Pass C: scatter.
   for (int i = tid; i < n_tiles; i += kSchedThreads) {
-    int s = seq_of(i);
-    int qt = i - tile_off[s];
+    const int s = seq_of(i);
+    const int qt = i - off_at(s);
     const int q0 = qt * entry_rows;
-    const int len = cu[s + 1] - cu[s];
-    const int offset = (cu_k[s + 1] - cu_k[s]) - len;
+    const int cs = cu_at(s), len = cu_at(s + 1) - cs;
+    const int cks = cuk_at(s), offset = (cuk_at(s + 1) - cks) - len;
     const int2 kr = qtile_key_range(q0, len, offset, window, entry_rows);
-    const int pos = atomicAdd(&s_cursor[min(kr.y, kCostBins) - 1], 1);
-    list[2 * pos] = make_int4(cu[s], q0, kr.x, len);
-    list[2 * pos + 1] = make_int4(cu_k[s], offset, kr.y, s);
+    const int pos = atomicAdd(&s_hist[min(kr.y, kCostBins) - 1], 1);
+    list[2 * pos] = make_int4(cs, q0, kr.x, len);
+    list[2 * pos + 1] = make_int4(cks, offset, kr.y, s);
   }
   if (tid == 0) ws[kWsNTiles] = n_tiles;
 }

@@ -365,9 +365,13 @@ void launch_attention(int D, int window, int qstep, int grid, const CUtensorMap&
 // it (the D = 128 kernel keeps computing it: there the extra state of the
 // bound spilled registers and cost 18-23%).  Returns the number of extra
 // blocks (0: no bound; too many KV heads).
-int key_norm_setup(tsk::KeyNorms* kn, const void* k, int64_t rows, int Hkv, int D, float* out) {
+int key_norm_setup(tsk::KeyNorms* kn, const void* k, int64_t rows, int Hkv, int D, int window,
+                   float* out) {
   *kn = tsk::KeyNorms{nullptr, 0, 0, 0, nullptr};
-  if (D != 64 || Hkv > tsk::kNormMaxHeads || rows <= 0) return 0;
+  // (the small-window softmax always computes its row maxima: no bound needed)
+  if (D != 64 || Hkv > tsk::kNormMaxHeads || rows <= 0 ||
+      (window > 0 && window <= tsk::kSmallWindowMax))
+    return 0;
   *kn = tsk::KeyNorms{reinterpret_cast<const uint4*>(k), (long long)rows, Hkv, D, out};
   // about four 16-byte chunks per thread, at most kNormBlocks blocks
   const int64_t want = (rows * Hkv * 8 + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads);
@@ -474,7 +478,7 @@ tsk_status prefill_impl(const void* q, const void* k, const void* v, const float
   float* knorm = reinterpret_cast<float*>(ws->base + off_ints + (size_t)ws->max_tiles * tsk::kTileEntryInts);
   tsk::KeyNorms kn;
   // (knorm_ext: bounds the caller computed over a larger key set)
-  const int norm_blocks = knorm_ext ? 0 : key_norm_setup(&kn, k, kv_rows, Hkv, D, knorm);
+  const int norm_blocks = knorm_ext ? 0 : key_norm_setup(&kn, k, kv_rows, Hkv, D, window, knorm);
   if (knorm_ext) kn = tsk::KeyNorms{nullptr, 0, 0, 0, nullptr};
   tsk::schedule_kernel<<<1 + norm_blocks, tsk::kSchedThreads, 0, stream>>>(
       cu_q, cu_k, num_seqs, (int)total_q, (int)total_k, window, ws->base, tile_off, list,
@@ -746,7 +750,7 @@ extern "C" tsk_status tsk_mha_prefill_noalloc(const void* q, const void* k, cons
   float* knorm = reinterpret_cast<float*>(scratch + kNoAllocOffInts +
                                           (size_t)kNoAllocMaxTiles * tsk::kTileEntryInts);
   tsk::KeyNorms kn;
-  const int norm_blocks = key_norm_setup(&kn, k, total_tokens, Hkv, D, knorm);
+  const int norm_blocks = key_norm_setup(&kn, k, total_tokens, Hkv, D, window, knorm);
   tsk::schedule_kernel<<<1 + norm_blocks, tsk::kSchedThreads, 0, stream>>>(
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, scratch,
       tile_off, list, kNoAllocMaxTiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM + qstep, kn);
@@ -1299,7 +1303,7 @@ extern "C" tsk_status tsk_mha_prefill_host(const void* q, const void* k, const v
     tsk::KeyNorms kn;
     int* n_ws = reinterpret_cast<int*>(b + off_n);  // [kWsNormCount] counter, then the norms
     float* n_out = reinterpret_cast<float*>(b + off_n) + 8;
-    const int nb = key_norm_setup(&kn, b + off_k, T, Hkv, D, n_out);
+    const int nb = key_norm_setup(&kn, b + off_k, T, Hkv, D, window, n_out);
     const float* d_knorm = nb ? n_out + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
     if (nb) {
       cudaMemcpyAsync(b + off_k, k, T * kvrow, cudaMemcpyHostToDevice, hp.h2d);
