@@ -101,7 +101,11 @@ __device__ void key_norm_blocks(const KeyNorms& kn, int* __restrict__ ws, int* s
   const long long stride = (long long)nblk * kSchedThreads;
   const unsigned group = 0xFFu << (tid & 24);  // the 8 lanes sharing this thread's row
   // kUnroll loads in flight per thread (enough bytes in flight to stream HBM)
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = 8;
+  // KV head of chunk i: (i / 8) % heads, kept incrementally (no 64-bit division
+  // in the loop): the stride is a multiple of 8 chunks.
+  const int hs = (int)((stride >> 3) % kn.heads);
+  int h0 = (int)((((long long)blk * kSchedThreads + tid) >> 3) % kn.heads);
   for (long long i0 = (long long)blk * kSchedThreads + tid; i0 < total; i0 += kUnroll * stride) {
     uint4 v[kUnroll];
 #pragma unroll
@@ -109,6 +113,7 @@ __device__ void key_norm_blocks(const KeyNorms& kn, int* __restrict__ ws, int* s
       const long long i = i0 + u * stride;
       v[u] = i < total ? __ldg(kn.k + i) : make_uint4(0u, 0u, 0u, 0u);
     }
+    int h = h0;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const long long i = i0 + u * stride;
@@ -124,8 +129,11 @@ __device__ void key_norm_blocks(const KeyNorms& kn, int* __restrict__ ws, int* s
       acc += __shfl_xor_sync(group, acc, 1);
       acc += __shfl_xor_sync(group, acc, 2);
       acc += __shfl_xor_sync(group, acc, 4);
-      if ((tid & 7) == 0) atomicMax(&s_max[(int)((i >> 3) % kn.heads)], __float_as_int(sqrtf(acc)));
+      if ((tid & 7) == 0) atomicMax(&s_max[h], __float_as_int(sqrtf(acc)));
+      h += hs;
+      if (h >= kn.heads) h -= kn.heads;
     }
+    h0 = (int)((h0 + (long long)kUnroll * hs) % kn.heads);
   }
   __syncthreads();
   for (int g = tid; g < kn.heads; g += kSchedThreads)

@@ -373,8 +373,9 @@ int key_norm_setup(tsk::KeyNorms* kn, const void* k, int64_t rows, int Hkv, int 
       (window > 0 && window <= tsk::kSmallWindowMax))
     return 0;
   *kn = tsk::KeyNorms{reinterpret_cast<const uint4*>(k), (long long)rows, Hkv, D, out};
-  // about four 16-byte chunks per thread, at most kNormBlocks blocks
-  const int64_t want = (rows * Hkv * 8 + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads);
+  // about eight 16-byte chunks per thread (one round of loads), at most
+  // kNormBlocks blocks
+  const int64_t want = (rows * Hkv * 8 + 8 * tsk::kSchedThreads - 1) / (8 * tsk::kSchedThreads);
   return (int)(want < tsk::kNormBlocks ? (want < 1 ? 1 : want) : tsk::kNormBlocks);
 }
 
