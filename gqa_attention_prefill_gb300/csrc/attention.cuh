@@ -399,6 +399,77 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
 #undef TSK_COMMIT
 }
 
+// One tcgen05.mma issuer for both query tiles (the small-window kernel, whose
+// units have few key tiles), in the order in which the softmax warpgroups
+// usually free S and publish P: S_0(0), S_1(0), S_0(1), S_1(1), then per key
+// tile j: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2).  Any other order of those
+// events only delays an MMA: each wait depends on MMAs issued before it.
+// Its commits are the only arrivals on the stage and Q release barriers.
+template <int QS>
+__device__ __forceinline__ void role_mma_pair(const Ctx& cx, const AttnParams& p) {
+  uint32_t q_iter = 0, kv_iter = 0;
+  uint32_t s_cnt[2] = {0u, 0u}, p_cnt[2] = {0u, 0u};
+  bool ok = true;
+  TSK_TL_DECL;
+  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    const Unit w = decode_unit<QS>(p, u);
+    const int qb = q_iter & 1;
+    const int nt = w.ntiles;
+    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3, p, cx.abort);
+    if (!ok) break;
+    auto issue_s = [&](int t, uint32_t kv) -> bool {
+      const int st = kv % kStages;
+      if (!mbar_wait(cx.bar(kBarKFull + st), (kv / kStages) & 1, 6, p, cx.abort)) return false;
+      if (s_cnt[t] > 0 &&
+          !mbar_wait(cx.bar(kBarSFree + t), (s_cnt[t] - 1) & 1, 5, p, cx.abort))
+        return false;
+      tc_fence_after();
+      const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes;
+      const uint32_t b = cx.sbase + kSmemKV + st * 2 * kTileBytes;
+      const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        mma_ss(d_s, sdesc_sw128(qaddr + 32 * kk), sdesc_sw128(b + 32 * kk), kIdescQK,
+               kk > 0 ? 1u : 0u);
+      tc_commit(cx.bar(kBarSFull + t));
+      ++s_cnt[t];
+      return true;
+    };
+    auto issue_pv = [&](int t, uint32_t kv, int j) -> bool {
+      const int st = kv % kStages;
+      if (!mbar_wait(cx.bar(kBarVFull + st), (kv / kStages) & 1, 7, p, cx.abort)) return false;
+      if (!mbar_wait(cx.bar(kBarPFull + t), p_cnt[t] & 1, 8, p, cx.abort)) return false;
+      tc_fence_after();
+      const uint32_t b = cx.sbase + kSmemKV + st * 2 * kTileBytes + kTileBytes;
+      const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
+      const uint32_t a_p = cx.tmem + kColP0 + 64 * t;
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_ts(d_o, a_p + 8 * kk, sdesc_sw128(b + 2048 * kk), kIdescPV,
+               (j > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(cx.bar(kBarPVDone + t));
+      ++p_cnt[t];
+      return true;
+    };
+    const int n = w.n_kv;
+    for (int t = 0; t < nt && ok; ++t) ok = issue_s(t, kv_iter);
+    for (int t = 0; t < nt && ok && n > 1; ++t) ok = issue_s(t, kv_iter + 1);
+    for (int j = 0; j < n && ok; ++j) {
+      for (int t = 0; t < nt && ok; ++t) {
+        ok = issue_pv(t, kv_iter + j, j);
+        if (ok && j + 2 < n) ok = issue_s(t, kv_iter + j + 2);
+      }
+      if (ok) tc_commit(cx.bar(kBarKVEmpty + (kv_iter + j) % kStages));
+    }
+    if (!ok) break;
+    kv_iter += n;
+    tc_commit(cx.bar(kBarQEmpty + qb));
+    ++q_iter;
+  }
+  tc_commit(cx.bar(kBarDrain));
+  mbar_wait<true>(cx.bar(kBarDrain), 0, 14, p, cx.abort);
+}
+
 // Column chunks of a 128-key tile (32 keys each) classified for one warp:
 // every row of the warp sees all keys of the chunk, none of them, or some.
 struct ChunkMask {
@@ -1004,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(cx.bar(kBarQFull + i), 1);
-      mbar_init(cx.bar(kBarQEmpty + i), 2);
+      mbar_init(cx.bar(kBarQEmpty + i), kSmallWindow ? 1 : 2);  // (one issuer, or one per tile)
       mbar_init(cx.bar(kBarSFull + i), 1);
       mbar_init(cx.bar(kBarSFree + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPFull + i), kSoftmaxWarpsPerTile);
@@ -1013,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(cx.bar(kBarKFull + s), 1);
       mbar_init(cx.bar(kBarVFull + s), 1);
-      mbar_init(cx.bar(kBarKVEmpty + s), 2);
+      mbar_init(cx.bar(kBarKVEmpty + s), kSmallWindow ? 1 : 2);
     }
     mbar_init(cx.bar(kBarDrain), 1);
     mbar_init(cx.bar(kBarDrain + 1), 1);
@@ -1046,8 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
 
   if (warp == 0 && lane == 0) role_producer<QS>(cx, &tmQ, &tmK, &tmV, p);
-  else if (warp == 1 && lane == 0) role_mma<QS>(cx, p, 0);
-  else if (warp == 2 && lane == 0) role_mma<QS>(cx, p, 1);
+  else if (kSmallWindow && warp == 1 && lane == 0) role_mma_pair<QS>(cx, p);
+  else if (!kSmallWindow && warp == 1 && lane == 0) role_mma<QS>(cx, p, 0);
+  else if (!kSmallWindow && warp == 2 && lane == 0) role_mma<QS>(cx, p, 1);
   else if (warp >= kFirstSoftmaxWarp) {
     if constexpr (kSmallWindow) role_softmax_window<QS>(cx, p, &tmO, warp, lane);
     else role_softmax_causal<QS>(cx, p, &tmO, warp, lane);
