@@ -500,10 +500,37 @@ __device__ __forceinline__ ChunkMask classify_chunks(int row0, int kbase, int wi
 // used for full causal attention and windows wider than kSmallWindowMax:
 // each row's 128 scores are held in registers for one pass (maximum, then
 // exponentials), edge tiles are masked per element, and each thread stores
-// its output row directly.
-template <int QS>
+// its output row directly.  L gives the shared-memory layout and the format of
+// the query tile (bf16 here; E4M3 in the FP8 kernel, which also scales the
+// output by out_scale).
+struct Bf16Layout {
+  static constexpr uint32_t kQ = kSmemQ, kQTile = kTileBytes, kEpi = kSmemEpi, kNorm = kSmemNorm;
+  static constexpr bool kScaleOut = false;
+  // Sum of squares of query row r of the (128-byte swizzled) bf16 tile at `tile`.
+  static __device__ __forceinline__ float q_sq(uint32_t tile, int r) {
+    // the row's 128 bytes (8 chunks of 16, permuted by the swizzle)
+    const uint32_t qrow = tile + (uint32_t)r * 128u;
+    float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      // chunk k ^ (r & 7): the lanes of a warp spread over all 32 banks
+      const uint4 v = ld_shared_v4(qrow + 16u * (uint32_t)(k ^ (r & 7)));
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+        ss[2 * e] = fmaf(lo, lo, ss[2 * e]);
+        ss[2 * e + 1] = fmaf(hi, hi, ss[2 * e + 1]);
+      }
+    }
+    return ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
+  }
+};
+
+template <int QS, class L = Bf16Layout>
 __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnParams& p,
-                                                    const CUtensorMap* tmO, int warp, int lane) {
+                                                    const CUtensorMap* tmO, int warp, int lane,
+                                                    float out_scale = 1.f) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;          // TMEM lane quarter
   const int r = wq * 32 + lane;     // query row within the tile
@@ -511,7 +538,7 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   const uint32_t tS = cx.tmem + lane_base + kColS0 + 128 * t;
   const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
   const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
-  const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
+  const uint32_t epi = cx.sbase + L::kEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
   uint32_t s_cnt = 0, pv_cnt = 0, q_iter = 0;
   TSK_TL_DECL;
@@ -565,23 +592,8 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
       if (!ok) break;
       TSK_EV(18);
-      // the row's 128 bytes (8 chunks of 16, permuted by the swizzle)
-      const uint32_t qrow = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes + (uint32_t)r * 128u;
-      float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        // chunk k ^ (r & 7): the lanes of a warp spread over all 32 banks
-        const uint4 v = ld_shared_v4(qrow + 16u * (uint32_t)(k ^ (r & 7)));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-          ss[2 * e] = fmaf(lo, lo, ss[2 * e]);
-          ss[2 * e + 1] = fmaf(hi, hi, ss[2 * e + 1]);
-        }
-      }
-      const float sq = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
-      bq = sl2 * sqrtf(sq) * cx.knorm_smem(gk);
+      const float sq = L::q_sq(cx.sbase + L::kQ + (2 * qb + t) * L::kQTile, r);
+      bq = sl2 * sqrtf(sq) * ld_shared_f32(cx.sbase + L::kNorm + 4u * (uint32_t)gk);
       TSK_EV(19);
     }
     // One key tile.  A slow tile computes its row maximum and raises the
@@ -757,7 +769,8 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     tmem_wait_ld();
     reg_fence<64>(o);
     TSK_EV(12);
-    const float inv = rcp_approx(l);
+    float inv = rcp_approx(l);
+    if constexpr (L::kScaleOut) inv *= out_scale;
     const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t ob[32];
 #pragma unroll

@@ -1,21 +1,21 @@
-// FP8 (E4M3) Q, K, V with per-tensor scales, head dimension 64: the D = 64
-// prefill design with 8-bit operands on the tensor cores.
+// FP8 (E4M3) Q, K, V with per-tensor scales, head dimension 64.
 //
 //   QK^T   tcgen05.mma kind::f8f6f4, M=128, N=128, K=32 per instruction (two
-//          per 64-column head); Q and K tiles are 128 rows of 64 bytes, stored
-//          by TMA with the 64-byte swizzle.
-//   PV     kind::f8f6f4 with P (E4M3, four per TMEM column) from TMEM and V^T
-//          from shared memory: both operands K-major.  V^T tiles (64 rows of
-//          128 keys) come from a transposed copy of V that fp8_vt_kernel
-//          writes per query tile of the schedule (each sequence's keys start
-//          on a 128-key boundary there, so every TMA box starts aligned;
-//          key rows past a sequence's end are zero).
-//   softmax as in the D = 64 kernel, with scale * q_scale * k_scale folded
-//          into the exponent and P rounded to E4M3 (P <= 2^8 < 448);
-//          O * v_scale / l in the epilogue.
-// TMEM: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384) P0 [384,416)
-//       P1 [416,448).
+//          per 64-column head): half the instructions and half the operand
+//          bytes of the bf16 kernel's QK^T.  Q and K tiles are 128 rows of 64
+//          bytes, stored by TMA with the 64-byte swizzle.
+//   PV     kind::f16 exactly as in the bf16 kernel: P in bf16 from TMEM, V
+//          from a bf16 copy of the E4M3 values that fp8_prep_kernel writes
+//          (exact: an E4M3 value has at most four significant bits); v_scale
+//          is applied in the epilogue.
+//   softmax  the bf16 kernel's (role_softmax_causal) with scale * q_scale *
+//          k_scale folded into the exponent, including its key-norm bound
+//          (the norms of the E4M3 key rows come from fp8_prep_kernel too), so
+//          the probabilities are bf16 and tiles may skip their row maximum.
+// TMEM columns and mbarriers as in the bf16 kernel.
 #pragma once
+#include <cuda_fp16.h>
+
 #include "attention.cuh"
 
 namespace tsk {
@@ -23,32 +23,14 @@ namespace fp8 {
 
 constexpr uint32_t kQTile = 128 * 64;  // bytes: 128 rows x 64 E4M3
 constexpr uint32_t kKTile = 128 * 64;
-constexpr uint32_t kVTile = 64 * 128;  // V^T: 64 rows (d) x 128 keys
-constexpr int kStages = 4;
+constexpr uint32_t kVTile = kTileBytes;  // bf16 V: 128 rows x 128 bytes
+constexpr uint32_t kStageBytes = kKTile + kVTile;
 constexpr uint32_t kSmemQ = 0;                                   // 2 buffers x 2 tiles
-constexpr uint32_t kSmemKV = 4 * kQTile;                         // kStages x (K, V^T)
-constexpr uint32_t kSmemEpi = kSmemKV + kStages * (kKTile + kVTile);  // 2 bf16 output tiles
-constexpr uint32_t kEpiTile = 128 * 64 * 2;
-constexpr uint32_t kSmemBar = kSmemEpi + 2 * kEpiTile;
-constexpr uint32_t kSmemBytes = kSmemBar + 512 + 1024;
-constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
-
-// Barrier slots (this kernel's ring is deeper than the bf16 kernel's).
-enum : int {
-  kBarQFull = 0,                 // [2]
-  kBarQEmpty = 2,                // [2]
-  kBarKFull = 4,                 // [kStages]
-  kBarVFull = 4 + kStages,       // [kStages]
-  kBarKVEmpty = 4 + 2 * kStages,
-  kBarSFull = 4 + 3 * kStages,   // [2]
-  kBarSFree = 6 + 3 * kStages,   // [2]
-  kBarPFull = 8 + 3 * kStages,   // [2]
-  kBarPVDone = 10 + 3 * kStages, // [2]
-  kBarDrain = 12 + 3 * kStages,  // [2]
-  kBarNever = 14 + 3 * kStages,
-  kNumBars = 15 + 3 * kStages
-};
-static_assert(8 * kNumBars + 8 <= 512, "barrier area");
+constexpr uint32_t kSmemKV = 4 * kQTile;                         // kStages x (K, V)
+constexpr uint32_t kSmemBar = kSmemKV + kStages * kStageBytes;   // barriers (< 512 B)
+constexpr uint32_t kSmemEpi = kSmemBar + 1024;                   // 2 bf16 output tiles
+constexpr uint32_t kSmemNorm = kSmemEpi + 2 * kTileBytes;        // key-norm bound per KV head
+constexpr uint32_t kSmemBytes = kSmemNorm + 4 * kNormMaxHeads + 1024;
 
 // Instruction descriptor, kind::f8f6f4: E4M3 A and B, fp32 accumulation,
 // both operands K-major.
@@ -57,7 +39,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 constexpr uint32_t kIdescQK = idesc_e4m3_f32(128, 128);
-constexpr uint32_t kIdescPV = idesc_e4m3_f32(128, 64);
 
 // Shared-memory descriptor: K-major rows of 64 bytes with the 64-byte swizzle
 // (8-row groups 512 bytes apart).
@@ -78,89 +59,125 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
-__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+
+// bf16 bit pattern of the OCP E4M3 code b (sign, 4 exponent bits with bias 7,
+// 3 mantissa bits; exponent 0 subnormal; S.1111.111 NaN), exact.
+__host__ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t b) {
+  const uint32_t sgn = (b & 0x80u) << 8;
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  if (e == 15u && m == 7u) return sgn | 0x7FC0u;
+  if (e != 0u) return sgn | ((e + 120u) << 7) | (m << 4);
+  if (m == 0u) return sgn;
+  // m * 2^-9 = 2^(-9 + msb) * (m / 2^msb): bf16 exponent field 118 + msb
+  const uint32_t msb = m >= 4u ? 2u : (m >= 2u ? 1u : 0u);
+  return sgn | ((118u + msb) << 7) | (((m << (7u - msb)) & 0x7Fu));
 }
 
-// Four fp32 values -> four E4M3 codes in one word (byte i = value i),
-// round to nearest even, saturating.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return (uint32_t)lo | ((uint32_t)hi << 16);
+// The E4M3 query tile: rows of 64 bytes, each within its own 64 bytes under the
+// 64-byte swizzle (only the order of its four 16-byte chunks changes).
+struct Layout {
+  static constexpr uint32_t kQ = kSmemQ, kQTile = fp8::kQTile, kEpi = kSmemEpi, kNorm = kSmemNorm;
+  static constexpr bool kScaleOut = true;  // (v_scale)
+  static __device__ __forceinline__ float q_sq(uint32_t tile, int r) {
+    const uint32_t qrow = tile + (uint32_t)r * 64u;
+    float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = ld_shared_v4(qrow + 16u * (uint32_t)((k + (r >> 1)) & 3));
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // two codes per conversion to f16x2 (exact; the order of the values
+        // does not matter for the norm)
+        uint32_t h01, h23;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(wv[e] & 0xFFFFu)));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(wv[e] >> 16)));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        ss[0] = fmaf(a.x, a.x, ss[0]);
+        ss[1] = fmaf(a.y, a.y, ss[1]);
+        ss[2] = fmaf(b.x, b.x, ss[2]);
+        ss[3] = fmaf(b.y, b.y, ss[3]);
+      }
+    }
+    return (ss[0] + ss[1]) + (ss[2] + ss[3]);
+  }
+};
+
+// V as bf16 ([rows, Hkv, 64], rows = tokens) and the per-KV-head maxima of the
+// E4M3 key-row norms, in one pass: four threads per 64-byte row, 16 codes each.
+// The per-block maxima and the last block's reduction use the key-norm buffer
+// and counter of the bf16 path (kn.out, ws[kWsNormCount]); with more than
+// kNormMaxHeads KV heads only V is converted (the kernel then has no bound).
+__global__ void __launch_bounds__(kSchedThreads, 1)
+    fp8_prep_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restrict__ v8,
+                    long long rows, int heads, uint4* __restrict__ vb, float* __restrict__ norm_out,
+                    int* __restrict__ ws) {
+  __shared__ int s_max[kNormMaxHeads];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
+  const int blk = blockIdx.x, nblk = gridDim.x;
+  const bool norms = heads <= kNormMaxHeads;
+  for (int g = tid; g < heads && norms; g += kSchedThreads) s_max[g] = 0;
+  __syncthreads();
+  const long long total = rows * heads * 4;  // 16-byte chunks
+  const long long stride = (long long)nblk * kSchedThreads;
+  const unsigned group = 0xFu << (tid & 28);  // the 4 lanes sharing this thread's row
+  for (long long i = (long long)blk * kSchedThreads + tid; i < total; i += stride) {
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k8) + i);
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(v8) + i);
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+    uint32_t ob[8];
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ob[2 * e] = e4m3_to_bf16_bits(vw[e] & 0xFFu) | (e4m3_to_bf16_bits((vw[e] >> 8) & 0xFFu) << 16);
+      ob[2 * e + 1] =
+          e4m3_to_bf16_bits((vw[e] >> 16) & 0xFFu) | (e4m3_to_bf16_bits(vw[e] >> 24) << 16);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const float x = __uint_as_float(e4m3_to_bf16_bits((kw[e] >> (8 * bb)) & 0xFFu) << 16);
+        acc = fmaf(x, x, acc);
+      }
+    }
+    vb[2 * i] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    vb[2 * i + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+    acc += __shfl_xor_sync(group, acc, 1);
+    acc += __shfl_xor_sync(group, acc, 2);
+    if ((tid & 3) == 0 && norms)  // (row index < 2^31: the host bounds tokens x heads)
+      atomicMax(&s_max[(unsigned)(i >> 2) % (unsigned)heads], __float_as_int(sqrtf(acc)));
+  }
+  if (!norms) return;
+  __syncthreads();
+  for (int g = tid; g < heads; g += kSchedThreads)
+    norm_out[blk * kNormMaxHeads + g] = __int_as_float(s_max[g]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&ws[kWsNormCount], 1) == nblk - 1;
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int g = tid; g < heads; g += kSchedThreads) s_max[g] = 0;
+    __syncthreads();
+    for (int i = tid; i < nblk * heads; i += kSchedThreads) {
+      const int b = i / heads, g = i - b * heads;
+      atomicMax(&s_max[g], __float_as_int(__ldcg(norm_out + b * kNormMaxHeads + g)));
+    }
+    __syncthreads();
+    for (int g = tid; g < heads; g += kSchedThreads)
+      norm_out[kNormBlocks * kNormMaxHeads + g] = __int_as_float(s_max[g]);
+    if (tid == 0) ws[kWsNormCount] = 0;
+  }
 }
 
 struct Fp8Params {
-  AttnParams a;         // as the bf16 kernels (out, lse, list, ws, status, heads, window)
-  const int* tile_off;  // [num_seqs + 1] query tiles before each sequence (schedule)
+  AttnParams a;  // as the bf16 kernels (out, lse, list, ws, status, heads, window, knorm)
   float v_scale;
-  // Extents checked by builds with -DTSK_DEBUG: sequences, V^T columns (keys).
-  int num_seqs = 0;
-  long long vt_cols = 0;
 };
 
-// Transposed V: vt[g][d][128 * i + r] = v[key r of query tile i][g][d] (zero
-// past the sequence's end), for every query tile i of the schedule.
-__global__ void __launch_bounds__(128)
-    fp8_vt_kernel(const uint8_t* __restrict__ v, const int* __restrict__ cu,
-                  const int* __restrict__ tile_off, const int* __restrict__ ws, int num_seqs,
-                  int Hkv, uint8_t* __restrict__ vt, int64_t t_pad) {
-  __shared__ __align__(16) uint8_t tile[128][64 + 16];
-  const int i = blockIdx.x, g = blockIdx.y;
-  if (i >= ws[kWsNTiles]) return;
-#ifdef TSK_DEBUG
-  if ((int64_t)(i + 1) * 128 > t_pad) {  // V^T too narrow for the tile list
-    if (atomicCAS(const_cast<int*>(ws) + kWsStatus, 0, -9) == 0) {
-      const_cast<int*>(ws)[kWsStatus + 1] = 50;
-      const_cast<int*>(ws)[kWsStatus + 2] = (int)blockIdx.x;
-    }
-    return;
-  }
-#endif
-  int lo = 0, hi = num_seqs - 1;  // the sequence owning tile i
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tile_off[mid] <= i) lo = mid;
-    else hi = mid - 1;
-  }
-  const int s = lo;
-  const int r = threadIdx.x;
-  const int key = (i - tile_off[s]) * 128 + r;
-  const int L = cu[s + 1] - cu[s];
-  uint4 row[4] = {};
-  if (key < L) {
-    const uint4* src = reinterpret_cast<const uint4*>(v + ((size_t)(cu[s] + key) * Hkv + g) * 64);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) row[c] = src[c];
-  }
-#pragma unroll
-  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(&tile[r][16 * c]) = row[c];
-  __syncthreads();
-  // Thread t writes 64 keys of row d = t / 2 of the transposed tile.
-  const int d = threadIdx.x >> 1, k0 = (threadIdx.x & 1) * 64;
-  uint8_t* dst = vt + ((size_t)g * 64 + d) * t_pad + (size_t)i * 128 + k0;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int kk = k0 + 16 * c + 4 * q;
-      w[q] = (uint32_t)tile[kk][d] | ((uint32_t)tile[kk + 1][d] << 8) |
-             ((uint32_t)tile[kk + 2][d] << 16) | ((uint32_t)tile[kk + 3][d] << 24);
-    }
-    *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* tmQ,
-                                              const CUtensorMap* tmK, const CUtensorMap* tmVt,
-                                              const Fp8Params& f) {
-  const AttnParams& p = f.a;
+                                              const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                              const AttnParams& p) {
   uint32_t q_iter = 0, kv_iter = 0;
   bool ok = true;
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
@@ -181,26 +198,21 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     }
     if (!ok) break;
     ++q_iter;
-    if (!TSK_IN_BOUNDS(p, cx.abort, w.seq >= 0 && w.seq < f.num_seqs, 47)) break;
-    const int vt_tile0 = __ldg(f.tile_off + w.seq);  // the sequence's first tile in V^T
     for (int j = 0; j < w.n_kv; ++j, ++kv_iter) {
       const int s = kv_iter % kStages;
       const uint32_t k = kv_iter / kStages;
       if (k >= 1) ok = mbar_wait(cx.bar(kBarKVEmpty + s), (k - 1) & 1, 2, p, cx.abort);
       if (!ok) break;
-      const int kt = w.kv_lo + j;
-      const uint32_t kdst = cx.sbase + kSmemKV + s * (kKTile + kVTile);
-      if (!TSK_IN_BOUNDS(p, cx.abort,
-                         w.g < p.Hkv && w.start_k + kt * kTileN < p.kv_rows &&
-                             (long long)(vt_tile0 + kt + 1) * 128 <= f.vt_cols,
-                         42)) {
+      const int row = w.start_k + (w.kv_lo + j) * kTileN;
+      const uint32_t kdst = cx.sbase + kSmemKV + s * kStageBytes;
+      if (!TSK_IN_BOUNDS(p, cx.abort, w.g < p.Hkv && row >= 0 && row < p.kv_rows, 42)) {
         ok = false;
         break;
       }
       mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kKTile);
-      tma_load_3d(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, w.start_k + kt * kTileN);
+      tma_load_3d(kdst, tmK, cx.bar(kBarKFull + s), 0, w.g, row);
       mbar_arrive_expect_tx(cx.bar(kBarVFull + s), kVTile);
-      tma_load_3d(kdst + kKTile, tmVt, cx.bar(kBarVFull + s), (vt_tile0 + kt) * 128, 0, w.g);
+      tma_load_3d(kdst + kKTile, tmV, cx.bar(kBarVFull + s), 0, w.g, row);
     }
   }
   for (uint32_t i = (kv_iter > kStages ? kv_iter - kStages : 0); i < kv_iter; ++i) {
@@ -211,13 +223,13 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     mbar_wait<true>(cx.bar(kBarQFull + (i & 1)), (i >> 1) & 1, 13, p, cx.abort);
 }
 
-// MMA issuer of query tile t (same protocol as the bf16 kernel).
+// MMA issuer of query tile t (the bf16 kernel's protocol and order).
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
   bool ok = true;
   const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
   const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
-  const uint32_t a_p = cx.tmem + kColP0 + 32 * t;
+  const uint32_t a_p = cx.tmem + kColP0 + 64 * t;
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     const int qb = q_iter & 1;
@@ -231,9 +243,9 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
     if (!ok) break;
     const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kQTile;
     auto issue_s = [&](int stage) {
-      const uint32_t b = cx.sbase + kSmemKV + stage * (kKTile + kVTile);
+      const uint32_t b = cx.sbase + kSmemKV + stage * kStageBytes;
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
+      for (int kk = 0; kk < 2; ++kk)  // 32 E4M3 elements per instruction
         mma_ss_f8(d_s, sdesc_sw64(qaddr + 32 * kk), sdesc_sw64(b + 32 * kk), kIdescQK,
                   kk > 0 ? 1u : 0u);
       tc_commit(cx.bar(kBarSFull + t));
@@ -262,11 +274,11 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       if (ok) ok = mbar_wait(cx.bar(kBarPFull + t), p_cnt & 1, 8, p, cx.abort);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t vb = cx.sbase + kSmemKV + sc * (kKTile + kVTile) + kKTile;
+      const uint32_t vb = cx.sbase + kSmemKV + sc * kStageBytes + kKTile;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // 32 keys per instruction
-        mma_ts_f8(d_o, a_p + 8 * kk, sdesc_sw128(vb + 32 * kk), kIdescPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_ts(d_o, a_p + 8 * kk, sdesc_sw128(vb + 2048 * kk), kIdescPV,
+               (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(cx.bar(kBarPVDone + t));
       ++p_cnt;
       for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarKVEmpty + sc));
@@ -280,198 +292,16 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   mbar_wait<true>(cx.bar(kBarDrain + t), 0, 14, p, cx.abort);
 }
 
-__device__ __forceinline__ void role_softmax(const Ctx& cx, const Fp8Params& f,
-                                             const CUtensorMap* tmO, int warp, int lane) {
-  const AttnParams& p = f.a;
-  const int t = (warp - kFirstSoftmaxWarp) >> 2;
-  const int wq = warp & 3;
-  const int r = wq * 32 + lane;
-  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-  const uint32_t tS = cx.tmem + lane_base + kColS0 + 128 * t;
-  const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
-  const uint32_t tP = cx.tmem + lane_base + kColP0 + 32 * t;
-  const uint32_t epi = cx.sbase + kSmemEpi + t * kEpiTile;
-  const float sl2 = p.scale_log2;  // scale * q_scale * k_scale * log2(e)
-  uint32_t s_cnt = 0, pv_cnt = 0;
-  bool ok = true;
-  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
-    int n_kv, kv_lo, diag0, pos;
-    float m_used = -INFINITY, l = 0.f;
-    {
-      const Unit w = decode_unit(p, u);
-      if (t >= w.ntiles) continue;
-      n_kv = w.n_kv;
-      kv_lo = w.kv_lo;
-      diag0 = w.offset + w.q0;
-      pos = diag0 + r;
-      if (p.sinks) {
-        if (TSK_IN_BOUNDS(p, cx.abort, w.h0 + t < p.Hq, 44))
-          m_used = __ldg(p.sinks + w.h0 + t) * 1.4426950408889634f;
-        l = 1.f;
-      }
-    }
-    for (int j = 0; j < n_kv; ++j) {
-      const int kt = kv_lo + j;
-      ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, 9, p, cx.abort);
-      if (!ok) break;
-      ++s_cnt;
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld_32x32b_x128(tS, sr);
-      tmem_wait_ld();
-      reg_fence<128>(sr);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-      const int kbase = kt * kTileN;
-      const bool edge = (kbase + kTileN - 1 > diag0) ||
-                        (p.window > 0 && kbase < diag0 + kTileM - p.window);
-      if (edge) {
-        const ChunkMask cm = classify_chunks(diag0 + wq * 32, kbase, p.window);
-        const int hi_c = pos - kbase;
-        const int lo_c = p.window > 0 ? pos - p.window + 1 - kbase : -1;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (cm.partial & (1u << k)) {
-#pragma unroll
-            for (int c = 32 * k; c < 32 * k + 32; ++c)
-              s[c] = (c > hi_c || c < lo_c) ? -INFINITY : s[c];
-          } else if (cm.none & (1u << k)) {
-#pragma unroll
-            for (int c = 32 * k; c < 32 * k + 32; ++c) s[c] = -INFINITY;
-          }
-        }
-      }
-      float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
-#pragma unroll
-      for (int c = 4; c < 128; c += 8) {
-        m0 = max3f(m0, s[c + 0], s[c + 1]);
-        m1 = max3f(m1, s[c + 2], s[c + 3]);
-        m2 = max3f(m2, s[c + 4], s[c + 5]);
-        m3 = max3f(m3, s[c + 6], s[c + 7]);
-      }
-      const float m_tile = max3f(m0, m1, fmaxf(m2, m3)) * sl2;
-      float alpha = 1.f;
-      if (__any_sync(0xffffffffu, m_tile > m_used + kRescaleThreshold)) {
-        if (m_tile > m_used) {
-          alpha = ex2_approx(m_used - m_tile);
-          m_used = m_tile;
-        }
-      }
-      l *= alpha;
-      const float m_use = m_used == -INFINITY ? 0.f : m_used;
-      // p = 2^(s*sl2 - m) <= 2^8, rounded to E4M3 for the PV operand; row
-      // sums in fp32.
-      uint32_t pk[32];
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t negm = f2_pack(-m_use, -m_use);
-      uint64_t acc2[2] = {0ull, 0ull};  // packed partial sums: one add per pair
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(s[4 * c], s[4 * c + 1]), sl2x2, negm), x0, x1);
-        f2_unpack(f2_fma(f2_pack(s[4 * c + 2], s[4 * c + 3]), sl2x2, negm), x2, x3);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        acc2[0] = f2_add(acc2[0], f2_pack(p0, p1));
-        acc2[1] = f2_add(acc2[1], f2_pack(p2, p3));
-        pk[c] = pack_e4m3x4(p0, p1, p2, p3);
-      }
-      {
-        float a0, a1, b0, b1;
-        f2_unpack(acc2[0], a0, a1);
-        f2_unpack(acc2[1], b0, b1);
-        l += (a0 + b0) + (a1 + b1);
-      }
-      if (j > 0) {
-        ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
-        if (!ok) break;
-        ++pv_cnt;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          uint32_t o[64];
-          tmem_ld_32x32b_x64(tO, o);
-          tmem_wait_ld();
-          reg_fence<64>(o);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st_32x32b_x64(tO, o);
-        }
-      }
-      tmem_st_32x32b_x32(tP, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
-    }
-    if (!ok) break;
-    // ------------------------------------------------------------ epilogue
-    const int per_tile = p.Hkv * p.HP;
-    const int qi = u / per_tile;
-    const int4 e = ld_nc_v4_volatile(p.list + 2 * qi);  // {start, q0, kv_lo, len}
-    const int g = (u - qi * per_tile) / p.HP;
-    const int h = g * p.G + 2 * (u - qi * per_tile - g * p.HP) + t;
-    ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
-    if (!ok) break;
-    ++pv_cnt;
-    tc_fence_after();
-    uint32_t o[64];
-    tmem_ld_32x32b_x64(tO, o);
-    tmem_wait_ld();
-    reg_fence<64>(o);
-    const float inv = f.v_scale * rcp_approx(l);
-    uint32_t ob[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      float a, b;
-      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1])),
-                       f2_pack(inv, inv)),
-                a, b);
-      ob[c] = pack_bf16x2(a, b);
-    }
-    const int row = e.y + r;
-    const size_t orow = (size_t)(e.x + row) * p.Hq + h;
-    // (rows past the sequence's end are neither stored nor checked)
-    const bool row_ok = row < e.w && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
-    if (p.lse && row_ok) p.lse[orow] = (m_used + lg2_approx(l)) * 0.69314718055994531f;
-    if (e.y + wq * 32 + 32 <= e.w) {
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
-      const uint32_t dst_row = epi + (uint32_t)r * 128u;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(dst_row + ((uint32_t)(c ^ (r & 7)) << 4), ob[4 * c], ob[4 * c + 1],
-                     ob[4 * c + 2], ob[4 * c + 3]);
-      fence_proxy_async_shared();
-      __syncwarp();
-      if (lane == 0 && TSK_IN_BOUNDS(p, cx.abort,
-                                     h < p.Hq && e.x + e.y + wq * 32 + 32 <= p.q_rows, 46)) {
-        tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, e.x + e.y + wq * 32);
-        bulk_commit_group();
-      }
-    } else if (row_ok) {
-      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * 64);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-    }
-    tc_fence_before();
-  }
-  if (lane == 0) bulk_wait_group0();
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ,
                              const __grid_constant__ CUtensorMap tmK,
-                             const __grid_constant__ CUtensorMap tmVt,
+                             const __grid_constant__ CUtensorMap tmV,
                              const __grid_constant__ CUtensorMap tmO,
                              const __grid_constant__ Fp8Params f) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const AttnParams& p = f.a;
   Ctx cx;
   cx.sbase = smem_u32(smem);
   cx.bar0 = cx.sbase + kSmemBar;
@@ -502,24 +332,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmVt);
+    tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  if (warp == 3 && p.knorm)
+    for (int g = lane; g < p.Hkv; g += 32) st_shared_f32(cx.sbase + kSmemNorm + 4u * g, __ldg(p.knorm + g));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   cx.tmem = *tmem_slot;
   cx.abort = smem_u32(const_cast<int*>(abort_flag));
-  cx.total_units = f.a.ws[kWsNTiles] * f.a.Hkv * f.a.HP;
+  cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
 
-  if (warp == 0 && lane == 0) fp8::role_producer(cx, &tmQ, &tmK, &tmVt, f);
-  else if (warp == 1 && lane == 0) fp8::role_mma(cx, f.a, 0);
-  else if (warp == 2 && lane == 0) fp8::role_mma(cx, f.a, 1);
-  else if (warp >= kFirstSoftmaxWarp) fp8::role_softmax(cx, f, &tmO, warp, lane);
+  if (warp == 0 && lane == 0) fp8::role_producer(cx, &tmQ, &tmK, &tmV, p);
+  else if (warp == 1 && lane == 0) fp8::role_mma(cx, p, 0);
+  else if (warp == 2 && lane == 0) fp8::role_mma(cx, p, 1);
+  else if (warp >= kFirstSoftmaxWarp)
+    role_softmax_causal<0, Layout>(cx, p, &tmO, warp, lane, f.v_scale);
 
   __syncwarp();
   tc_fence_before();

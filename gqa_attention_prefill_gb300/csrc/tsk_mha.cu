@@ -33,8 +33,8 @@ struct Workspace {
   int max_seqs = 0;
   float* part = nullptr;  // decode: per-split partial states
   size_t part_bytes = 0;
-  uint8_t* vt = nullptr;  // FP8 prefill: transposed V
-  size_t vt_bytes = 0;
+  uint8_t* fp8_v = nullptr;  // FP8 prefill: V as bf16 values
+  size_t fp8_v_bytes = 0;
 };
 
 struct DeviceState {
@@ -108,20 +108,6 @@ tsk_status encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int D,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? TSK_OK : TSK_ERR_DEVICE;
-}
-
-// A 3-D uint8 tensor (innermost first) with a box of box0 x box1 x 1 and the
-// given swizzle.
-tsk_status encode_u8(CUtensorMap* m, const void* ptr, const cuuint64_t dims[3],
-                     const cuuint64_t strides[2], cuuint32_t box0, cuuint32_t box1,
-                     CUtensorMapSwizzle swz) {
-  cuuint32_t box[3] = {box0, box1, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr),
-                        const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides), box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TSK_OK : TSK_ERR_DEVICE;
 }
 
@@ -615,7 +601,7 @@ tsk_status tsk_release(void) {
       if (it != g_ws.end()) {
         if (it->second.base) cudaFree(it->second.base);
         if (it->second.part) cudaFree(it->second.part);
-        if (it->second.vt) cudaFree(it->second.vt);
+        if (it->second.fp8_v) cudaFree(it->second.fp8_v);
         g_ws.erase(it);
       }
       if (st) cudaStreamDestroy(st);
@@ -626,7 +612,7 @@ tsk_status tsk_release(void) {
     if (kv.second.base || kv.second.part) cudaSetDevice(kv.first.first);
     if (kv.second.base) cudaFree(kv.second.base);
     if (kv.second.part) cudaFree(kv.second.part);
-    if (kv.second.vt) cudaFree(kv.second.vt);
+    if (kv.second.fp8_v) cudaFree(kv.second.fp8_v);
   }
   if (dev >= 0) cudaSetDevice(dev);
   g_ws.clear();
@@ -1033,19 +1019,18 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   const int max_tiles = (int)max_tiles64;
   Workspace* ws = nullptr;
   if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
-  // Transposed V: [Hkv][64][t_pad] bytes, t_pad = 128 x (query-tile bound).
-  const int64_t t_pad = (int64_t)ws->max_tiles * 128;
-  const size_t vt_need = (size_t)Hkv * 64 * (size_t)t_pad;
-  if (ws->vt_bytes < vt_need) {
+  // V as bf16 values, [total_tokens, Hkv, 64] (the PV operand).
+  const size_t vb_need = (size_t)total_tokens * Hkv * 64 * 2;
+  if (ws->fp8_v_bytes < vb_need) {
     uint8_t* nb = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), vt_need, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "FP8 V^T buffer");
-    if (ws->vt) cudaFreeAsync(ws->vt, stream);
-    ws->vt = nb;
-    ws->vt_bytes = vt_need;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), vb_need, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "FP8 bf16 V buffer");
+    if (ws->fp8_v) cudaFreeAsync(ws->fp8_v, stream);
+    ws->fp8_v = nb;
+    ws->fp8_v_bytes = vb_need;
   }
 
-  CUtensorMap tq, tk, tvt, to;
+  CUtensorMap tq, tk, tv, to;
   {
     const cuuint64_t dq[3] = {64, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
     const cuuint64_t sq[2] = {64, (cuuint64_t)Hq * 64};
@@ -1064,10 +1049,7 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return TSK_ERR_DEVICE;
-    const cuuint64_t dv[3] = {(cuuint64_t)t_pad, 64, (cuuint64_t)Hkv};
-    const cuuint64_t sv[2] = {(cuuint64_t)t_pad, (cuuint64_t)t_pad * 64};
-    if ((st = encode_u8(&tvt, ws->vt, dv, sv, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != TSK_OK)
-      return st;
+    if ((st = encode_thd(&tv, ws->fp8_v, total_tokens, Hkv, 64)) != TSK_OK) return st;
     if ((st = encode_thd(&to, out, total_tokens, Hq, 64, 32)) != TSK_OK) return st;
   }
 
@@ -1098,9 +1080,15 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, ws->base,
       tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM,
       tsk::KeyNorms{nullptr, 0, 0, 0, nullptr});
-  tsk::fp8::fp8_vt_kernel<<<dim3(max_tiles, Hkv), 128, 0, stream>>>(
-      reinterpret_cast<const uint8_t*>(v8), cu_seqlens, tile_off, ws->base, num_seqs, Hkv, ws->vt,
-      t_pad);
+  // bf16 V and the E4M3 key-row norms (at most kNormBlocks blocks, about four
+  // 16-byte chunks of each tensor per thread)
+  float* knorm = reinterpret_cast<float*>(ws->base + off_ints + (size_t)ws->max_tiles * tsk::kTileEntryInts);
+  const int heads_ok = Hkv <= tsk::kNormMaxHeads;
+  int prep_blocks = (int)((total_tokens * Hkv * 4 + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads));
+  prep_blocks = prep_blocks < 1 ? 1 : (prep_blocks > tsk::kNormBlocks ? tsk::kNormBlocks : prep_blocks);
+  tsk::fp8::fp8_prep_kernel<<<prep_blocks, tsk::kSchedThreads, 0, stream>>>(
+      reinterpret_cast<const uint8_t*>(k8), reinterpret_cast<const uint8_t*>(v8),
+      (long long)total_tokens, Hkv, reinterpret_cast<uint4*>(ws->fp8_v), knorm, ws->base);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
   tsk::fp8::Fp8Params f;
@@ -1123,14 +1111,12 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   p.q_rows = (int)total_tokens;
   p.kv_rows = (int)total_tokens;
   p.max_tiles = ws->max_tiles;
-  f.tile_off = tile_off;
-  f.num_seqs = num_seqs;
-  f.vt_cols = t_pad;
+  p.knorm = heads_ok ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
   f.v_scale = v_scale;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
   tsk::fp8::attention_fwd_fp8_kernel<<<grid, tsk::kThreads, tsk::fp8::kSmemBytes, stream>>>(
-      tq, tk, tvt, to, f);
+      tq, tk, tv, to, f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) note_error("FP8 attention kernel launch", e);
   if (prof) {

@@ -1,18 +1,17 @@
 """FP8 (E4M3) prefill against the CPU oracle on the exact dequantised inputs,
 through the C ABI.
 
-P is rounded to E4M3 before the PV product: three mantissa bits, round to
-nearest, so the error of a probability p is at most p / 16, or half the
-subnormal spacing 2^-10 below 2^-6 (the kernel's p is relative to a running
-maximum no larger than the row's, so 2^-10 also bounds it relative to the
-row maximum).  Hence for every output element
-|out - exact| <= sum_j max(p_j / 16, 2^-10) |v_j| / l + bf16 rounding.  Every
+The scores come from E4M3 Q and K with fp32 accumulation (exact products);
+P is rounded to bf16 before the PV product with V's values in bf16 (exact
+for E4M3 values): eight significant bits, round to nearest, so the error of
+a probability p is at most p / 256 relative to whatever maximum the kernel
+subtracts.  Hence for every output element
+|out - exact| <= sum_j (p_j / 256) |v_j| / l + bf16 rounding of out.  Every
 test checks exactly that bound per element: on every row of the small cases,
 and on the >= 4096 sampled rows of the full-size workload (the bound is
 computed here in float64 from the same dequantised inputs, only for the rows
-compared).  The mean error of the cases with many keys per row is also held to 5e-3
-(about 10x the bf16 path's).
-LSE comes from fp32 sums and keeps the 1e-3 bar."""
+compared).  The mean error of the cases with many keys per row is held to
+the bf16 path's 2e-3.  LSE comes from fp32 sums and keeps the 1e-3 bar."""
 import numpy as np
 import pytest
 
@@ -22,7 +21,7 @@ import parity
 
 pytestmark = pytest.mark.gpu
 LSE_MAX = 1e-3
-MEAN_MAX = 5e-3
+MEAN_MAX = 2e-3
 
 
 
@@ -56,7 +55,7 @@ def run_fp8(w, with_lse=True):
 
 
 def p_rounding_bound(w):
-    """sum_j max(p_j / 16, 2^-10) |v_j| / l per output element, float64 (small cases)."""
+    """sum_j (p_j / 256) |v_j| / l per output element, float64 (small cases)."""
     q = inputgen.bf16_bits_to_f32(w.q).astype(np.float64)
     k = inputgen.bf16_bits_to_f32(w.k).astype(np.float64)
     v = inputgen.bf16_bits_to_f32(w.v).astype(np.float64)
@@ -74,7 +73,7 @@ def p_rounding_bound(w):
             m = np.maximum(sc.max(axis=1), sink)
             pr = np.exp(sc - m[:, None])
             l = pr.sum(axis=1) + np.exp(sink - m)
-            err_p = np.where(ok, np.maximum(pr / 16, 2.0 ** -10), 0.0)
+            err_p = np.where(ok, pr / 256, 0.0)
             bound[a:a + L, h] = (err_p @ np.abs(v[a:a + L, g])) / l[:, None]
     return bound
 
@@ -98,7 +97,7 @@ def p_rounding_bound_rows(w, t, h):
         m = max(sc.max(), sink)
         pr = np.exp(sc - m)
         l = pr.sum() + np.exp(sink - m)
-        bound[i] = (np.maximum(pr / 16, 2.0 ** -10) @ vv) / l
+        bound[i] = ((pr / 256) @ vv) / l
     return bound
 
 
