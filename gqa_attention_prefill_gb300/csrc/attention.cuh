@@ -227,10 +227,6 @@ struct Ctx {
   int total_units;
   uint32_t abort;   // shared address of the CTA's abort flag
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
-  // Largest key-row norm of KV head g (copied to shared memory at the start).
-  __device__ __forceinline__ float knorm_smem(int g) const {
-    return ld_shared_f32(sbase + kSmemNorm + 4u * (uint32_t)g);
-  }
 };
 
 
