@@ -95,7 +95,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
 }
 
 // cu_k must be 0 = cu_k[0] < cu_k[1] < ... with every length 1 .. max_k and
-// cu_k[num_seqs] = total_k.  Writes this call's verdict to *bad and, on
+// cu_k[num_seqs] = total_k.  Writes this call's result to *bad and, on
 // failure, TSK_ERR_BAD_SEQLENS (-8) to the sticky status word.  Also clears
 // the n_counters split counters of this call.
 __global__ void decode_check_kernel(const int* cu_k, int num_seqs, int total_k, int max_k,
