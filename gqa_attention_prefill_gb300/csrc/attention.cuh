@@ -838,6 +838,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
   const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
   uint32_t s_cnt = 0, pv_cnt = 0;
+  TSK_TL_DECL;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
   // The next unit and its sink are loaded before a unit's epilogue, so that
@@ -854,6 +855,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
   float sink_n = -INFINITY;
   fetch(blockIdx.x, wn, sink_n);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+    TSK_EV(8);
     const Unit w = wn;
     const float sink = sink_n;
     if (t >= w.ntiles) {
@@ -867,8 +869,10 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     float m_used = sink, l = sink == -INFINITY ? 0.f : 1.f;
     for (int j = 0; j < w.n_kv; ++j) {
       const int kt = w.kv_lo + j;
+      TSK_EV(1);
       ok = mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort);
       if (!ok) break;
+      TSK_EV(2);
       ++s_cnt;
       tc_fence_after();
       const int kbase = kt * kTileN;
@@ -977,10 +981,12 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
         l += (a0 + b0) + (a1 + b1);
         TSK_TRACE_ADD(22, tr_exp);
       }
+      TSK_EV(5);
       if (j > 0) {
         // O_t is stable and P_t reusable once PV_t(j-1) has completed.
         ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort);
         if (!ok) break;
+        TSK_EV(6);
         ++pv_cnt;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -1003,13 +1009,16 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
+      TSK_EV(7);
     }
     if (!ok) break;
     fetch(u + gridDim.x, wn, sink_n);
+    TSK_EV(9);
     // ------------------------------------------------------------ epilogue
     TSK_TRACE_T0(tr_epi);
     ok = mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 25, p, cx.abort);
     if (!ok) break;
+    TSK_EV(10);
     ++pv_cnt;
     tc_fence_after();
     uint32_t o[64];
