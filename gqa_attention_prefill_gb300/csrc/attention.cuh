@@ -95,6 +95,8 @@ struct AttnParams {
   // Extents checked by builds with -DTSK_DEBUG: rows of q/out, rows of the
   // k/v buffers (tokens, or slots of a paged pool), capacity of the tile list.
   int q_rows = 0, kv_rows = 0, max_tiles = 0;
+  // Factor applied to the output (the value scale of E4M3 inputs; D = 128 kernel).
+  float out_scale = 1.f;
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.

@@ -21,6 +21,11 @@
 //          swizzled rows (one TMA box each).
 //   epilogue  two passes of 64 output columns per warp through its staging
 //          slice and a TMA bulk tensor store.
+//   E4M3 inputs (kFp8): Q and K tiles are 128 rows of 128 E4M3 bytes (one
+//          TMA box, 128-byte swizzle, in the first half of each bf16 slot),
+//          QK^T is four kind::f8f6f4 MMAs (K = 32) instead of eight; V comes
+//          as bf16 values (exact) from the FP8 pre-pass, and the output is
+//          multiplied by p.out_scale (the value scale).
 #pragma once
 #include "attention.cuh"
 
@@ -41,6 +46,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP = 64;  // P at S_t + kColP
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescQK8 = idesc_e4m3_f32(128, 128);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
 
 enum : int {
@@ -74,7 +80,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo)
 }
 
 // TMA producer (one thread).
-template <int QS>
+template <int QS, bool kFp8>
 __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* tmQ,
                                               const CUtensorMap* tmK, const CUtensorMap* tmV,
                                               const AttnParams& p) {
@@ -86,14 +92,14 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
     const Unit w = decode_unit<QS>(p, u);
     if (q_iter >= 1) ok = mbar_wait(cx.bar(kBarQEmpty), (q_iter - 1) & 1, 1, p, cx.abort);
     if (!ok) break;
-    mbar_arrive_expect_tx(cx.bar(kBarQFull), w.ntiles * kTile);
+    mbar_arrive_expect_tx(cx.bar(kBarQFull), w.ntiles * (kFp8 ? kHalf : kTile));
     for (int t = 0; t < w.ntiles && ok; ++t) {
       const int h = tile_head<QS>(w, t), row = w.start + tile_q0<QS>(w, t);
       if (!TSK_IN_BOUNDS(p, cx.abort, h >= 0 && h < p.Hq && row >= 0 && row < p.q_rows, 41)) {
         ok = false;
         break;
       }
-      for (int hf = 0; hf < 2; ++hf)
+      for (int hf = 0; hf < (kFp8 ? 1 : 2); ++hf)
         tma_load_3d(cx.sbase + kSmemQ + t * kTile + hf * kHalf, tmQ, cx.bar(kBarQFull), 64 * hf,
                     h, row);
     }
@@ -117,9 +123,9 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kTile);
+        mbar_arrive_expect_tx(cx.bar(kBarKFull + s), kFp8 ? kHalf : kTile);
         bool in = true;
-        for (int hf = 0; hf < 2; ++hf)
+        for (int hf = 0; hf < (kFp8 ? 1 : 2); ++hf)
           in = tma_load_key_rows(dst + hf * kHalf, tmK, cx.bar(kBarKFull + s), 64 * hf, w.g,
                                  p.kv, w.seq, w.start_k, pos0, Lk) && in;
         if (!TSK_IN_BOUNDS(p, cx.abort, in, 43)) {
@@ -160,7 +166,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
 // tcgen05.mma issuer for query tile t (one thread).  The release barriers
 // (Q, K and V buffers) count one arrival per tile; for a unit with a single
 // query tile, tile 0 arrives twice.
-template <int QS>
+template <int QS, bool kFp8>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, p_cnt = 0;
   bool ok = true;
@@ -184,10 +190,18 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       const int s = it % kStagesKV;
       const uint32_t kb = cx.sbase + kSmemKV + s * 2 * kTile;
       TSK_TRACE_T0(tr_is);
+      if constexpr (kFp8) {
 #pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalf + 32 * (kk & 3);
-        mma_ss(d_s, sdesc_sw128(q_addr + off), sdesc_sw128(kb + off), kIdescQK, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kD / 32; ++kk)  // 32 E4M3 bytes per instruction
+          mma_ss_f8(d_s, sdesc_sw128(q_addr + 32 * kk), sdesc_sw128(kb + 32 * kk), kIdescQK8,
+                    kk > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + 32 * (kk & 3);
+          mma_ss(d_s, sdesc_sw128(q_addr + off), sdesc_sw128(kb + off), kIdescQK,
+                 kk > 0 ? 1u : 0u);
+        }
       }
       tc_commit(cx.bar(kBarSFull + t));
       release(kBarKEmpty + s);
@@ -239,7 +253,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
 }
 
 // Softmax and epilogue of query tile t (one warpgroup, one thread per row).
-template <int QS>
+template <int QS, bool kFp8>
 __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
                                              const CUtensorMap* tmO, int warp, int lane) {
   const int t = (warp - kFirstSoftmaxWarp) >> 2;
@@ -407,7 +421,8 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
     // (rows past the sequence's end are neither stored nor checked)
     const bool row_ok = row < e.w && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
     if (p.lse && row_ok) p.lse[orow] = (m_used + log2f(l)) * 0.69314718055994531f;
-    const float inv = rcp_approx(l);
+    float inv = rcp_approx(l);
+    if constexpr (kFp8) inv *= p.out_scale;
     const bool staged = e.y + wq * 32 + 32 <= e.w;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -449,7 +464,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
   if (lane == 0) bulk_wait_group0();  // every output store of this warp has completed
 }
 
-template <int QS>
+template <int QS, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ,
                               const __grid_constant__ CUtensorMap tmK,
@@ -514,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // between neighbouring splits.)
   if (warp < kFirstSoftmaxWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
-    if (warp == 0 && lane == 0) d128::role_producer<QS>(cx, &tmQ, &tmK, &tmV, p);
-    else if (warp == 1 && lane == 0) d128::role_mma<QS>(cx, p, 0);
-    else if (warp == 2 && lane == 0) d128::role_mma<QS>(cx, p, 1);
+    if (warp == 0 && lane == 0) d128::role_producer<QS, kFp8>(cx, &tmQ, &tmK, &tmV, p);
+    else if (warp == 1 && lane == 0) d128::role_mma<QS, kFp8>(cx, p, 0);
+    else if (warp == 2 && lane == 0) d128::role_mma<QS, kFp8>(cx, p, 1);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
-    d128::role_softmax<QS>(cx, p, &tmO, warp, lane);
+    d128::role_softmax<QS, kFp8>(cx, p, &tmO, warp, lane);
   }
 
   __syncwarp();

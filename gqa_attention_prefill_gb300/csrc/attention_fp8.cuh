@@ -32,12 +32,6 @@ constexpr uint32_t kSmemEpi = kSmemBar + 1024;                   // 2 bf16 outpu
 constexpr uint32_t kSmemNorm = kSmemEpi + 2 * kTileBytes;        // key-norm bound per KV head
 constexpr uint32_t kSmemBytes = kSmemNorm + 4 * kNormMaxHeads + 1024;
 
-// Instruction descriptor, kind::f8f6f4: E4M3 A and B, fp32 accumulation,
-// both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
 constexpr uint32_t kIdescQK = idesc_e4m3_f32(128, 128);
 
 // Shared-memory descriptor: K-major rows of 64 bytes with the 64-byte swizzle
@@ -52,25 +46,19 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
-// bf16 bit pattern of the OCP E4M3 code b (sign, 4 exponent bits with bias 7,
-// 3 mantissa bits; exponent 0 subnormal; S.1111.111 NaN), exact.
-__host__ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t b) {
-  const uint32_t sgn = (b & 0x80u) << 8;
-  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-  if (e == 15u && m == 7u) return sgn | 0x7FC0u;
-  if (e != 0u) return sgn | ((e + 120u) << 7) | (m << 4);
-  if (m == 0u) return sgn;
-  // m * 2^-9 = 2^(-9 + msb) * (m / 2^msb): bf16 exponent field 118 + msb
-  const uint32_t msb = m >= 4u ? 2u : (m >= 2u ? 1u : 0u);
-  return sgn | ((118u + msb) << 7) | (((m << (7u - msb)) & 0x7Fu));
+// The four E4M3 codes of w (byte i = element i) as floats, exactly (E4M3 ->
+// f16 is exact; f16 -> f32 too).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float& x0, float& x1, float& x2,
+                                              float& x3) {
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(w & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(w >> 16)));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  x0 = a.x;
+  x1 = a.y;
+  x2 = b.x;
+  x3 = b.y;
 }
 
 // The E4M3 query tile: rows of 64 bytes, each within its own 64 bytes under the
@@ -87,64 +75,62 @@ struct Layout {
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        // two codes per conversion to f16x2 (exact; the order of the values
-        // does not matter for the norm)
-        uint32_t h01, h23;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(wv[e] & 0xFFFFu)));
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(wv[e] >> 16)));
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-        ss[0] = fmaf(a.x, a.x, ss[0]);
-        ss[1] = fmaf(a.y, a.y, ss[1]);
-        ss[2] = fmaf(b.x, b.x, ss[2]);
-        ss[3] = fmaf(b.y, b.y, ss[3]);
+        float x0, x1, x2, x3;
+        e4m3x4_to_f32(wv[e], x0, x1, x2, x3);
+        ss[0] = fmaf(x0, x0, ss[0]);
+        ss[1] = fmaf(x1, x1, ss[1]);
+        ss[2] = fmaf(x2, x2, ss[2]);
+        ss[3] = fmaf(x3, x3, ss[3]);
       }
     }
     return (ss[0] + ss[1]) + (ss[2] + ss[3]);
   }
 };
 
-// V as bf16 ([rows, Hkv, 64], rows = tokens) and the per-KV-head maxima of the
-// E4M3 key-row norms, in one pass: four threads per 64-byte row, 16 codes each.
+// V as bf16 ([rows, Hkv, D], rows = tokens; chunks_per_row = D / 16) and, if
+// norms (D = 64), the per-KV-head maxima of the E4M3 key-row norms, in one
+// pass: four threads per 64-byte key row, 16 codes each.
 // The per-block maxima and the last block's reduction use the key-norm buffer
 // and counter of the bf16 path (kn.out, ws[kWsNormCount]); with more than
 // kNormMaxHeads KV heads only V is converted (the kernel then has no bound).
 __global__ void __launch_bounds__(kSchedThreads, 1)
     fp8_prep_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restrict__ v8,
-                    long long rows, int heads, uint4* __restrict__ vb, float* __restrict__ norm_out,
-                    int* __restrict__ ws) {
+                    long long rows, int heads, int chunks_per_row, bool norms,
+                    uint4* __restrict__ vb, float* __restrict__ norm_out, int* __restrict__ ws) {
   __shared__ int s_max[kNormMaxHeads];
   __shared__ int s_last;
   const int tid = threadIdx.x;
   const int blk = blockIdx.x, nblk = gridDim.x;
-  const bool norms = heads <= kNormMaxHeads;
+  // (norms: 64-byte key rows, at most kNormMaxHeads heads)
   for (int g = tid; g < heads && norms; g += kSchedThreads) s_max[g] = 0;
   __syncthreads();
-  const long long total = rows * heads * 4;  // 16-byte chunks
+  const long long total = rows * heads * chunks_per_row;  // 16-byte chunks
   const long long stride = (long long)nblk * kSchedThreads;
   const unsigned group = 0xFu << (tid & 28);  // the 4 lanes sharing this thread's row
   for (long long i = (long long)blk * kSchedThreads + tid; i < total; i += stride) {
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k8) + i);
+    const uint4 kv = norms ? __ldg(reinterpret_cast<const uint4*>(k8) + i) : make_uint4(0, 0, 0, 0);
     const uint4 vv = __ldg(reinterpret_cast<const uint4*>(v8) + i);
     const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
     uint32_t ob[8];
     float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      ob[2 * e] = e4m3_to_bf16_bits(vw[e] & 0xFFu) | (e4m3_to_bf16_bits((vw[e] >> 8) & 0xFFu) << 16);
-      ob[2 * e + 1] =
-          e4m3_to_bf16_bits((vw[e] >> 16) & 0xFFu) | (e4m3_to_bf16_bits(vw[e] >> 24) << 16);
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        const float x = __uint_as_float(e4m3_to_bf16_bits((kw[e] >> (8 * bb)) & 0xFFu) << 16);
-        acc = fmaf(x, x, acc);
+      float v0, v1, v2, v3;
+      e4m3x4_to_f32(vw[e], v0, v1, v2, v3);
+      ob[2 * e] = pack_bf16x2(v0, v1);  // (exact: at most four significant bits)
+      ob[2 * e + 1] = pack_bf16x2(v2, v3);
+      if (norms) {
+        float k0, k1, k2, k3;
+        e4m3x4_to_f32(kw[e], k0, k1, k2, k3);
+        acc = fmaf(k0, k0, fmaf(k1, k1, fmaf(k2, k2, fmaf(k3, k3, acc))));
       }
     }
     vb[2 * i] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
     vb[2 * i + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+    if (!norms) continue;
     acc += __shfl_xor_sync(group, acc, 1);
     acc += __shfl_xor_sync(group, acc, 2);
-    if ((tid & 3) == 0 && norms)  // (row index < 2^31: the host bounds tokens x heads)
+    if ((tid & 3) == 0)  // (row index < 2^31: the host bounds tokens x heads)
       atomicMax(&s_max[(unsigned)(i >> 2) % (unsigned)heads], __float_as_int(sqrtf(acc)));
   }
   if (!norms) return;

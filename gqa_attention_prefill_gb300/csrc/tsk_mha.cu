@@ -156,6 +156,10 @@ tsk_status check_device(int* dev_out, DeviceState** st_out) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::d128::kSmemBytes);
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tsk::d128::attention_fwd_d128_kernel<0, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tsk::d128::kSmemBytes);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tsk::fp8::attention_fwd_fp8_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tsk::fp8::kSmemBytes);
@@ -994,7 +998,7 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
   for (float x : {scale, q_scale, k_scale, v_scale})
     if (!std::isfinite(x) || !(x > 0.f)) return TSK_ERR_INVALID_ARG;
-  if (D != 64 || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
+  if ((D != 64 && D != 128) || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
   if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
     return TSK_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
@@ -1019,8 +1023,8 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   const int max_tiles = (int)max_tiles64;
   Workspace* ws = nullptr;
   if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
-  // V as bf16 values, [total_tokens, Hkv, 64] (the PV operand).
-  const size_t vb_need = (size_t)total_tokens * Hkv * 64 * 2;
+  // V as bf16 values, [total_tokens, Hkv, D] (the PV operand).
+  const size_t vb_need = (size_t)total_tokens * Hkv * D * 2;
   if (ws->fp8_v_bytes < vb_need) {
     uint8_t* nb = nullptr;
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), vb_need, stream);
@@ -1032,25 +1036,28 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
 
   CUtensorMap tq, tk, tv, to;
   {
-    const cuuint64_t dq[3] = {64, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
-    const cuuint64_t sq[2] = {64, (cuuint64_t)Hq * 64};
-    const cuuint64_t dk[3] = {64, (cuuint64_t)Hkv, (cuuint64_t)total_tokens};
-    const cuuint64_t sk[2] = {64, (cuuint64_t)Hkv * 64};
-    // Q/K boxes: 64 bytes x 1 head x 128 rows (the second box dimension is the head)
-    cuuint32_t box[3] = {64, 1, 128};
+    const cuuint64_t dq[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
+    const cuuint64_t sq[2] = {(cuuint64_t)D, (cuuint64_t)Hq * D};
+    const cuuint64_t dk[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)total_tokens};
+    const cuuint64_t sk[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
+    // Q/K boxes: one whole row of D bytes x 1 head x 128 rows (the second box
+    // dimension is the head); 64-byte rows use the 64-byte swizzle, 128-byte
+    // rows the 128-byte one.
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle swz = D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     CUresult r = g_encode(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q8),
                           const_cast<cuuint64_t*>(dq), const_cast<cuuint64_t*>(sq), box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r == CUDA_SUCCESS)
       r = g_encode(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(k8),
                    const_cast<cuuint64_t*>(dk), const_cast<cuuint64_t*>(sk), box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return TSK_ERR_DEVICE;
-    if ((st = encode_thd(&tv, ws->fp8_v, total_tokens, Hkv, 64)) != TSK_OK) return st;
-    if ((st = encode_thd(&to, out, total_tokens, Hq, 64, 32)) != TSK_OK) return st;
+    if ((st = encode_thd(&tv, ws->fp8_v, total_tokens, Hkv, D)) != TSK_OK) return st;
+    if ((st = encode_thd(&to, out, total_tokens, Hq, D, 32)) != TSK_OK) return st;
   }
 
   char name[112];
@@ -1080,15 +1087,17 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
       cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, ws->base,
       tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM,
       tsk::KeyNorms{nullptr, 0, 0, 0, nullptr});
-  // bf16 V and the E4M3 key-row norms (at most kNormBlocks blocks, about four
-  // 16-byte chunks of each tensor per thread)
+  // bf16 V and, for D = 64, the E4M3 key-row norms (at most kNormBlocks
+  // blocks, about four 16-byte chunks of each tensor per thread)
   float* knorm = reinterpret_cast<float*>(ws->base + off_ints + (size_t)ws->max_tiles * tsk::kTileEntryInts);
-  const int heads_ok = Hkv <= tsk::kNormMaxHeads;
-  int prep_blocks = (int)((total_tokens * Hkv * 4 + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads));
+  const bool norms = D == 64 && Hkv <= tsk::kNormMaxHeads;
+  const int chunks = D / 16;
+  int prep_blocks = (int)((total_tokens * Hkv * chunks + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads));
   prep_blocks = prep_blocks < 1 ? 1 : (prep_blocks > tsk::kNormBlocks ? tsk::kNormBlocks : prep_blocks);
   tsk::fp8::fp8_prep_kernel<<<prep_blocks, tsk::kSchedThreads, 0, stream>>>(
       reinterpret_cast<const uint8_t*>(k8), reinterpret_cast<const uint8_t*>(v8),
-      (long long)total_tokens, Hkv, reinterpret_cast<uint4*>(ws->fp8_v), knorm, ws->base);
+      (long long)total_tokens, Hkv, chunks, norms, reinterpret_cast<uint4*>(ws->fp8_v), knorm,
+      ws->base);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
   tsk::fp8::Fp8Params f;
@@ -1111,12 +1120,17 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   p.q_rows = (int)total_tokens;
   p.kv_rows = (int)total_tokens;
   p.max_tiles = ws->max_tiles;
-  p.knorm = heads_ok ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
+  p.knorm = norms ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
+  p.out_scale = v_scale;
   f.v_scale = v_scale;
   const int64_t units_bound = max_tiles64 * Hkv * p.HP;
   const int grid = (int)(units_bound < ds->num_sms ? units_bound : ds->num_sms);
-  tsk::fp8::attention_fwd_fp8_kernel<<<grid, tsk::kThreads, tsk::fp8::kSmemBytes, stream>>>(
-      tq, tk, tv, to, f);
+  if (D == 64)
+    tsk::fp8::attention_fwd_fp8_kernel<<<grid, tsk::kThreads, tsk::fp8::kSmemBytes, stream>>>(
+        tq, tk, tv, to, f);
+  else
+    tsk::d128::attention_fwd_d128_kernel<0, true>
+        <<<grid, tsk::kThreads, tsk::d128::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) note_error("FP8 attention kernel launch", e);
   if (prof) {

@@ -197,14 +197,14 @@ TSK_API tsk_status tsk_mha_decode_paged(const void *q, const void *k_pages, cons
  * bytes) whose values are code * q_scale, code * k_scale, code * v_scale
  * (per-tensor fp32 scales, finite and > 0).  The result is the attention of
  * those values (scale, sinks, window, lse and out as in tsk_mha_prefill; out
- * stays bf16).  Head dimension 64 only.  Q K^T runs on E4M3 operands with
+ * stays bf16).  Head dimension 64 or 128.  Q K^T runs on E4M3 operands with
  * fp32 accumulation; P is rounded to bf16 for the PV product, whose V
  * operand is V's values in bf16 (exact), so outputs differ from the exact
  * attention of the dequantised inputs by up to sum_j (p_j / 256) |v_j| / l
  * per element plus bf16 rounding, as in tsk_mha_prefill.  Three launches:
- * the scheduler, a pre-pass (V as bf16, key-row norms), the attention.  Extra
- * device memory per (device, stream): total_tokens * Hkv * 128 bytes for V
- * in bf16.
+ * the scheduler, a pre-pass (V as bf16; for D = 64 also the key-row norms),
+ * the attention.  Extra device memory per (device, stream):
+ * total_tokens * Hkv * D * 2 bytes for V in bf16.
  */
 TSK_API tsk_status tsk_mha_prefill_fp8(const void *q8, const void *k8, const void *v8,
                                       float q_scale, float k_scale, float v_scale,

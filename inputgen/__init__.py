@@ -289,6 +289,8 @@ CONFIGS = {
     # FP8 (E4M3) Q/K/V with per-tensor scales, otherwise the bench workload
     "fp8_causal_4x4096_h64kv8": dict(desc="as causal_4x4096 with E4M3 Q/K/V (per-tensor "
                                           "power-of-two scales)"),
+    "fp8_causal_4x4096_h32kv8_d128": dict(desc="as causal_4x4096_h32kv8_d128 with E4M3 Q/K/V "
+                                               "(per-tensor power-of-two scales)"),
     # head dimension 128 (the same unmasked FLOPs as causal_4x4096_h64kv8)
     "causal_4x4096_h32kv8_d128": dict(desc="4 seqs x 4096 tokens, Hq=32, Hkv=8, D=128, "
                                            "sinks N(0,1), scale 1/sqrt(128), full causal"),
@@ -327,6 +329,8 @@ def config(name: str, seed: int = 0) -> Workload:
                             seed=seed, name=name)
     if name == "fp8_causal_4x4096_h64kv8":
         return make_fp8([4096] * 4, 64, 8, seed=seed, name=name)
+    if name == "fp8_causal_4x4096_h32kv8_d128":
+        return make_fp8([4096] * 4, 32, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
     if name == "causal_4x4096_h32kv8_d128":
         return make([4096] * 4, 32, 8, D=128, scale=128 ** -0.5, seed=seed, name=name)
     if name == "long_1x32768_h32kv8_d128":

@@ -127,6 +127,20 @@ def test_small_cases_within_the_rounding_bound(seqlens, window):
     assert np.abs(lse - rl).max() <= LSE_MAX
 
 
+@pytest.mark.parametrize("seqlens,window", [([1], 0), ([129, 3, 300], 0), ([400, 257], 100),
+                                             ([500], 1)])
+def test_head_dim_128_within_the_rounding_bound(seqlens, window):
+    w = inputgen.make_fp8(seqlens, 8, 2, D=128, window=window, scale=128 ** -0.5,
+                          seed=sum(seqlens) + window + 128)
+    out, lse = run_fp8(w)
+    ro, rl, _ = oracle.run_workload(w)
+    b = p_rounding_bound(w)
+    err = check_within_bound(out, ro, b, f"D=128 L={seqlens} W={window}", mean_max=None)
+    print(f"D=128 L={seqlens} W={window}: out max {err.max():.3g} mean {err.mean():.3g} "
+          f"(bound max {b.max():.3g}), lse max {np.abs(lse - rl).max():.3g}")
+    assert np.abs(lse - rl).max() <= LSE_MAX
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 1), (6, 2), (64, 8)])
 def test_head_groupings(Hq, Hkv):
     w = inputgen.make_fp8([333, 129], Hq, Hkv, seed=Hq + Hkv)
@@ -145,8 +159,9 @@ def test_no_sinks_no_lse():
     check_within_bound(out, ro, p_rounding_bound(w), "no sinks")
 
 
-def test_bench_config_sampled():
-    w = inputgen.config("fp8_causal_4x4096_h64kv8")
+@pytest.mark.parametrize("name", ["fp8_causal_4x4096_h64kv8", "fp8_causal_4x4096_h32kv8_d128"])
+def test_bench_config_sampled(name):
+    w = inputgen.config(name)
     out, lse = run_fp8(w)
     t, h = inputgen.sample_rows(w, n_target=4096)
     assert len(t) >= 4096
@@ -155,7 +170,7 @@ def test_bench_config_sampled():
     assert np.isfinite(out).all()
     o = out[t, h]
     b = p_rounding_bound_rows(w, t, h)
-    err = check_within_bound(o, ro, b, f"fp8 bench config [{len(t)} rows]")
-    print(f"fp8 bench config [{len(t)} rows]: out max {err.max():.3g} mean {err.mean():.3g} "
+    err = check_within_bound(o, ro, b, f"{name} [{len(t)} rows]")
+    print(f"{name} [{len(t)} rows]: out max {err.max():.3g} mean {err.mean():.3g} "
           f"(bound max {b.max():.3g}), lse max {np.abs(lse[t, h] - rl).max():.3g}")
     assert np.abs(lse[t, h] - rl).max() <= LSE_MAX
