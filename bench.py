@@ -72,7 +72,8 @@ def kernel_source_hash(D=64, decode=False, fp8=False):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_attention_prefill_gb300", "csrc")
     files = ["ptx.cuh", "schedule.cuh", "attention.cuh"]
-    files += (["decode.cuh"] if decode else ["attention_fp8.cuh"] if fp8 else
+    files += (["decode.cuh"] if decode else
+              ["attention_fp8.cuh"] + (["attention_d128.cuh"] if D == 128 else []) if fp8 else
               ["attention_d128.cuh"] if D == 128 else [])
     for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
@@ -475,6 +476,7 @@ def main():
     kernel_s = attn_avg * 1e-3
     alg_bytes = w.algorithmic_bytes()
     kernel_name = ("decode_split_kernel<%d> (merging its splits)" % D if decode else
+                   "attention_fwd_d128_kernel<0, true> (E4M3 Q/K)" if fp8 and D == 128 else
                    "attention_fwd_fp8_kernel" if fp8 else
                    "attention_fwd_d128_kernel" if D == 128 else
                    "attention_fwd_kernel<true>" if 0 < w.window <= 512 else
