@@ -70,7 +70,10 @@ constexpr uint32_t kSmemEpi = kSmemBar + 1024;  // 2 output staging tiles
 constexpr uint32_t kSmemNorm = kSmemEpi + 2 * kTileBytes;  // key-norm bound per KV head
 // Dynamic shared memory per kernel variant, + 1 KB slack for the alignment.
 constexpr uint32_t kSmemBytesCausal = kSmemNorm + 4 * kNormMaxHeads + 1024;
-constexpr uint32_t kSmemBytesWindow = kSmemNorm + 4 * kNormMaxHeads + 1024;
+// (the small-window kernel has no key-norm bound; a second set of output
+// staging tiles takes that region and more)
+constexpr uint32_t kSmemBytesWindow = kSmemEpi + 4 * kTileBytes + 1024;
+static_assert(kSmemBytesWindow <= 227 * 1024, "shared memory budget");
 
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
 constexpr uint32_t kTmemCols = 512;
@@ -840,6 +843,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
   const uint32_t epi = cx.sbase + kSmemEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
   uint32_t s_cnt = 0, pv_cnt = 0;
+  uint32_t n_staged = 0;  // staged output stores of this warp (two staging buffers)
   TSK_TL_DECL;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
@@ -1027,6 +1031,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     tmem_ld_32x32b_x64(tO, o);
     tmem_wait_ld();
     reg_fence<64>(o);
+    TSK_EV(12);
     const float inv = rcp_approx(l);
     const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t ob[32];
@@ -1041,21 +1046,27 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     // (rows past the sequence's end are neither stored nor checked)
     const bool row_ok = row < w.len && TSK_IN_BOUNDS(p, cx.abort, orow < (size_t)p.q_rows * p.Hq, 45);
     if (p.lse && row_ok) p.lse[orow] = (m_used + lg2_approx(l)) * 0.69314718055994531f;
+    TSK_EV(13);
     if (q0t + wq * 32 + 32 <= w.len) {
       // The warp's 32 rows lie inside the sequence: stage them in this warp's
       // slice of the staging tile and store them with one TMA bulk store.
-      if (lane == 0) bulk_wait_group_read0();  // the warp's previous store has read its slice
+      // two staging buffers: the store that used this one (two units ago)
+      // has read it once at most one store group is still reading
+      const uint32_t epb = epi + ((n_staged++ & 1u) ? 2u * kTileBytes : 0u);
+      if (lane == 0) bulk_wait_group_read1();
       __syncwarp();
-      const uint32_t dst_row = epi + (uint32_t)r * 128u;
+      TSK_EV(14);
+      const uint32_t dst_row = epb + (uint32_t)r * 128u;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         st_shared_v4(dst_row + ((uint32_t)(c ^ (r & 7)) << 4), ob[4 * c], ob[4 * c + 1],
                      ob[4 * c + 2], ob[4 * c + 3]);
       fence_proxy_async_shared();
       __syncwarp();
+      TSK_EV(15);
       if (lane == 0 && TSK_IN_BOUNDS(p, cx.abort,
                                      h < p.Hq && w.start + q0t + wq * 32 + 32 <= p.q_rows, 46)) {
-        tma_store_3d(tmO, epi + (uint32_t)wq * 4096u, 0, h, w.start + q0t + wq * 32);
+        tma_store_3d(tmO, epb + (uint32_t)wq * 4096u, 0, h, w.start + q0t + wq * 32);
         bulk_commit_group();
       }
     } else if (row_ok) {
@@ -1065,6 +1076,7 @@ __device__ __forceinline__ void role_softmax_window(const Ctx& cx, const AttnPar
     }
     tc_fence_before();
     TSK_TRACE_ADD(28, tr_epi);
+    TSK_EV(11);
   }
   if (lane == 0) bulk_wait_group0();  // every output store of this warp has completed
   TSK_TRACE_ADD(30, tr_all);
