@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = ["tsk_mha_prefill", "tsk_mha_prefill_noalloc", "tsk_mha_prefill_kvcache",
-           "tsk_mha_decode_kvcache", "tsk_mha_prefill_paged", "tsk_mha_decode_paged", "tsk_mha_prefill_fp8", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
+           "tsk_mha_decode_kvcache", "tsk_mha_prefill_paged", "tsk_mha_decode_paged", "tsk_mha_prefill_fp8", "tsk_mha_prefill_fp8_kvcache", "mha_prefill", "mha_prefill_kvcache", "mha_decode_kvcache",
            "tsk_get_device_status", "tsk_noalloc_status", "tsk_status_string",
            "tsk_last_error", "tsk_debug_set_wait",
            "tsk_profile_enable", "tsk_profile_read", "tsk_release", "tsk_kernels_per_call",
@@ -94,6 +94,9 @@ def load_library():
         lib.tsk_mha_prefill_fp8.argtypes = [P, P, P, f32, f32, f32, P, P, i32, i64, i32, i32, i32,
                                             i32, f32, P, P, P]
         lib.tsk_mha_prefill_fp8.restype = ctypes.c_int
+        lib.tsk_mha_prefill_fp8_kvcache.argtypes = [P, P, P, f32, f32, f32, P, P, P, i32, i64,
+                                                    i64, i32, i32, i32, i32, f32, P, P, P]
+        lib.tsk_mha_prefill_fp8_kvcache.restype = ctypes.c_int
         lib.tsk_status_string.argtypes = [ctypes.c_int]
         lib.tsk_status_string.restype = ctypes.c_char_p
         lib.tsk_last_error.argtypes = []
@@ -250,6 +253,19 @@ def tsk_mha_prefill_fp8(q8, k8, v8, q_scale, k_scale, v_scale, sinks, cu_seqlens
                                    float(v_scale), _ptr(sinks), _ptr(cu_seqlens), int(num_seqs),
                                    int(total_tokens), int(Hq), int(Hkv), int(D), int(window),
                                    float(scale), _ptr(out), _ptr(lse), _stream_handle(stream))
+
+
+def tsk_mha_prefill_fp8_kvcache(q8, k8, v8, q_scale, k_scale, v_scale, sinks, cu_seqlens_q,
+                                cu_seqlens_k, num_seqs, total_q, total_k, Hq, Hkv, D, window,
+                                scale, out, lse, stream=None) -> int:
+    """E4M3 prefill over a contiguous key/value cache (same arguments as the C
+    function).  Returns the status."""
+    lib = load_library()
+    return lib.tsk_mha_prefill_fp8_kvcache(
+        _ptr(q8), _ptr(k8), _ptr(v8), float(q_scale), float(k_scale), float(v_scale),
+        _ptr(sinks), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(num_seqs), int(total_q),
+        int(total_k), int(Hq), int(Hkv), int(D), int(window), float(scale), _ptr(out), _ptr(lse),
+        _stream_handle(stream))
 
 
 def mha_decode_kvcache(q, k, v, cu_seqlens_k, max_seqlen_k: int, sinks=None, window: int = 0,

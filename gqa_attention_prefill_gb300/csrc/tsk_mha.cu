@@ -987,31 +987,37 @@ extern "C" tsk_status tsk_mha_decode_paged(const void* q, const void* k_pages, c
 
 // ---------------------------------------------------------------------------
 // FP8 (E4M3) prefill, head dimension 64.
-extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const void* v8,
-                                          float q_scale, float k_scale, float v_scale,
-                                          const float* sinks, const int32_t* cu_seqlens,
-                                          int32_t num_seqs, int64_t total_tokens, int32_t Hq,
-                                          int32_t Hkv, int32_t D, int32_t window, float scale,
-                                          void* out, float* lse, tsk_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (!q8 || !k8 || !v8 || !out || !cu_seqlens) return TSK_ERR_INVALID_ARG;
-  if (num_seqs < 0 || total_tokens < 0 || Hq <= 0 || Hkv <= 0) return TSK_ERR_INVALID_ARG;
+namespace {
+// FP8 prefill over keys that may extend before the queries (cu_k == cu_q and
+// total_k == total_q for plain prefill).
+tsk_status prefill_fp8_impl(const void* q8, const void* k8, const void* v8, float q_scale,
+                            float k_scale, float v_scale, const float* sinks,
+                            const int32_t* cu_seqlens, const int32_t* cu_k, int32_t num_seqs,
+                            int64_t total_tokens, int64_t total_k, int32_t Hq, int32_t Hkv,
+                            int32_t D, int32_t window, float scale, void* out, float* lse,
+                            cudaStream_t stream, const char* what) {
+  if (!q8 || !k8 || !v8 || !out || !cu_seqlens || !cu_k) return TSK_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || total_k < 0 || Hq <= 0 || Hkv <= 0)
+    return TSK_ERR_INVALID_ARG;
   for (float x : {scale, q_scale, k_scale, v_scale})
     if (!std::isfinite(x) || !(x > 0.f)) return TSK_ERR_INVALID_ARG;
   if ((D != 64 && D != 128) || Hq % Hkv != 0) return TSK_ERR_UNSUPPORTED;
-  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31))
+  if (num_seqs >= (1 << 24) || total_tokens * (int64_t)Hq >= ((int64_t)1 << 31) ||
+      total_k * (int64_t)Hkv * D >= ((int64_t)1 << 31) || total_k >= ((int64_t)1 << 31))
     return TSK_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; };
   if (!a16(q8) || !a16(k8) || !a16(v8) || !a16(out)) return TSK_ERR_ALIGNMENT;
-  if (!a4(cu_seqlens) || (sinks && !a4(sinks)) || (lse && !a4(lse))) return TSK_ERR_ALIGNMENT;
+  if (!a4(cu_seqlens) || !a4(cu_k) || (sinks && !a4(sinks)) || (lse && !a4(lse)))
+    return TSK_ERR_ALIGNMENT;
   const size_t out_bytes = (size_t)total_tokens * Hq * D * 2;
-  const size_t q_bytes = (size_t)total_tokens * Hq * D, kv_bytes = (size_t)total_tokens * Hkv * D;
+  const size_t q_bytes = (size_t)total_tokens * Hq * D, kv_bytes = (size_t)total_k * Hkv * D;
   if (total_tokens > 0 && (overlaps(out, out_bytes, q8, q_bytes) ||
                            overlaps(out, out_bytes, k8, kv_bytes) ||
                            overlaps(out, out_bytes, v8, kv_bytes)))
     return TSK_ERR_INVALID_ARG;
   if (num_seqs == 0 || total_tokens == 0) return TSK_OK;
+  if (total_k < total_tokens) return TSK_ERR_INVALID_ARG;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = -1;
@@ -1023,8 +1029,8 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   const int max_tiles = (int)max_tiles64;
   Workspace* ws = nullptr;
   if ((st = get_workspace(dev, stream, max_tiles, num_seqs, &ws)) != TSK_OK) return st;
-  // V as bf16 values, [total_tokens, Hkv, D] (the PV operand).
-  const size_t vb_need = (size_t)total_tokens * Hkv * D * 2;
+  // V as bf16 values, [total_k, Hkv, D] (the PV operand).
+  const size_t vb_need = (size_t)total_k * Hkv * D * 2;
   if (ws->fp8_v_bytes < vb_need) {
     uint8_t* nb = nullptr;
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nb), vb_need, stream);
@@ -1038,7 +1044,7 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   {
     const cuuint64_t dq[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
     const cuuint64_t sq[2] = {(cuuint64_t)D, (cuuint64_t)Hq * D};
-    const cuuint64_t dk[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)total_tokens};
+    const cuuint64_t dk[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)total_k};
     const cuuint64_t sk[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
     // Q/K boxes: one whole row of D bytes x 1 head x 128 rows (the second box
     // dimension is the head); 64-byte rows use the 64-byte swizzle, 128-byte
@@ -1056,13 +1062,13 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return TSK_ERR_DEVICE;
-    if ((st = encode_thd(&tv, ws->fp8_v, total_tokens, Hkv, D)) != TSK_OK) return st;
+    if ((st = encode_thd(&tv, ws->fp8_v, total_k, Hkv, D)) != TSK_OK) return st;
     if ((st = encode_thd(&to, out, total_tokens, Hq, D, 32)) != TSK_OK) return st;
   }
 
   char name[112];
-  snprintf(name, sizeof name, "tsk_mha_prefill_fp8[Hq=%d,Hkv=%d,W=%d,nseq=%d,T=%lld]", Hq, Hkv,
-           window, num_seqs, (long long)total_tokens);
+  snprintf(name, sizeof name, "%s[Hq=%d,Hkv=%d,W=%d,nseq=%d,T=%lld,Tk=%lld]", what, Hq, Hkv,
+           window, num_seqs, (long long)total_tokens, (long long)total_k);
   nvtxRangePushA(name);
   const size_t off_ints = ((size_t)tsk::kWsHeader + (size_t)ws->max_seqs + 1 + 3) & ~(size_t)3;
   int* tile_off = ws->base + tsk::kWsHeader;
@@ -1084,7 +1090,7 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
     cudaEventRecord(g_ev[0], stream);
   }
   tsk::schedule_kernel<<<1, tsk::kSchedThreads, 0, stream>>>(
-      cu_seqlens, cu_seqlens, num_seqs, (int)total_tokens, (int)total_tokens, window, ws->base,
+      cu_seqlens, cu_k, num_seqs, (int)total_tokens, (int)total_k, window, ws->base,
       tile_off, list, ws->max_tiles, tsk::PagedKV{nullptr, 0, 0, 0}, tsk::kTileM,
       tsk::KeyNorms{nullptr, 0, 0, 0, nullptr});
   // bf16 V and, for D = 64, the E4M3 key-row norms (at most kNormBlocks
@@ -1092,11 +1098,11 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   float* knorm = reinterpret_cast<float*>(ws->base + off_ints + (size_t)ws->max_tiles * tsk::kTileEntryInts);
   const bool norms = D == 64 && Hkv <= tsk::kNormMaxHeads;
   const int chunks = D / 16;
-  int prep_blocks = (int)((total_tokens * Hkv * chunks + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads));
+  int prep_blocks = (int)((total_k * Hkv * chunks + 4 * tsk::kSchedThreads - 1) / (4 * tsk::kSchedThreads));
   prep_blocks = prep_blocks < 1 ? 1 : (prep_blocks > tsk::kNormBlocks ? tsk::kNormBlocks : prep_blocks);
   tsk::fp8::fp8_prep_kernel<<<prep_blocks, tsk::kSchedThreads, 0, stream>>>(
       reinterpret_cast<const uint8_t*>(k8), reinterpret_cast<const uint8_t*>(v8),
-      (long long)total_tokens, Hkv, chunks, norms, reinterpret_cast<uint4*>(ws->fp8_v), knorm,
+      (long long)total_k, Hkv, chunks, norms, reinterpret_cast<uint4*>(ws->fp8_v), knorm,
       ws->base);
   if (prof) cudaEventRecord(g_ev[1], stream);
 
@@ -1118,7 +1124,7 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   p.debug_stall = g_debug_stall;
   p.kv = tsk::PagedKV{nullptr, 0, 0, 0};
   p.q_rows = (int)total_tokens;
-  p.kv_rows = (int)total_tokens;
+  p.kv_rows = (int)total_k;
   p.max_tiles = ws->max_tiles;
   p.knorm = norms ? knorm + tsk::kNormBlocks * tsk::kNormMaxHeads : nullptr;
   p.out_scale = v_scale;
@@ -1139,6 +1145,31 @@ extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const 
   }
   nvtxRangePop();
   return e == cudaSuccess ? TSK_OK : TSK_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+}  // namespace
+
+extern "C" tsk_status tsk_mha_prefill_fp8(const void* q8, const void* k8, const void* v8,
+                                          float q_scale, float k_scale, float v_scale,
+                                          const float* sinks, const int32_t* cu_seqlens,
+                                          int32_t num_seqs, int64_t total_tokens, int32_t Hq,
+                                          int32_t Hkv, int32_t D, int32_t window, float scale,
+                                          void* out, float* lse, tsk_stream_t stream) {
+  return prefill_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, sinks, cu_seqlens, cu_seqlens,
+                          num_seqs, total_tokens, total_tokens, Hq, Hkv, D, window, scale, out,
+                          lse, reinterpret_cast<cudaStream_t>(stream), "tsk_mha_prefill_fp8");
+}
+
+extern "C" tsk_status tsk_mha_prefill_fp8_kvcache(
+    const void* q8, const void* k8, const void* v8, float q_scale, float k_scale, float v_scale,
+    const float* sinks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+    int32_t num_seqs, int64_t total_q, int64_t total_k, int32_t Hq, int32_t Hkv, int32_t D,
+    int32_t window, float scale, void* out, float* lse, tsk_stream_t stream) {
+  return prefill_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, sinks, cu_seqlens_q,
+                          cu_seqlens_k, num_seqs, total_q, total_k, Hq, Hkv, D, window, scale,
+                          out, lse, reinterpret_cast<cudaStream_t>(stream),
+                          "tsk_mha_prefill_fp8_kvcache");
 }
 
 // ---------------------------------------------------------------------------

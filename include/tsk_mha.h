@@ -213,6 +213,26 @@ TSK_API tsk_status tsk_mha_prefill_fp8(const void *q8, const void *k8, const voi
                                       int32_t Hkv, int32_t D, int32_t window, float scale,
                                       void *out, float *lse, tsk_stream_t stream);
 
+/*
+ * tsk_mha_prefill_fp8_kvcache -- tsk_mha_prefill_fp8 over a contiguous key/value
+ * cache: the arguments of tsk_mha_prefill_kvcache (per-sequence query and key
+ * offsets cu_seqlens_q / cu_seqlens_k, Lk >= Lq, query i of a sequence at key
+ * position Lk - Lq + i) with E4M3 q8 [total_q, Hq, D], k8 and v8
+ * [total_k, Hkv, D] and the per-tensor scales of tsk_mha_prefill_fp8.
+ * Head dimension 64 or 128; the same accuracy bound as tsk_mha_prefill_fp8;
+ * total_k >= total_q (else TSK_ERR_INVALID_ARG); offsets are checked on the
+ * device (TSK_ERR_BAD_SEQLENS through tsk_get_device_status).  Extra device
+ * memory per (device, stream): total_k * Hkv * D * 2 bytes for V in bf16.
+ */
+TSK_API tsk_status tsk_mha_prefill_fp8_kvcache(const void *q8, const void *k8, const void *v8,
+                                              float q_scale, float k_scale, float v_scale,
+                                              const float *sinks, const int32_t *cu_seqlens_q,
+                                              const int32_t *cu_seqlens_k, int32_t num_seqs,
+                                              int64_t total_q, int64_t total_k, int32_t Hq,
+                                              int32_t Hkv, int32_t D, int32_t window,
+                                              float scale, void *out, float *lse,
+                                              tsk_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 TSK_API const char *tsk_status_string(tsk_status s);
 

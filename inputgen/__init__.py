@@ -266,6 +266,31 @@ def make_kvcache(q_lens, k_lens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0, s
                     cu_seqlens_k=cu_k, seqlens_k=k_lens)
 
 
+def make_kvcache_fp8(q_lens, k_lens, Hq, Hkv, D=64, window=0, scale=0.125, seed=0,
+                     sink_sigma=1.0, with_sinks=True, name="kvcache_fp8") -> Workload:
+    """`make_kvcache` with Q, K, V drawn in fp32 and quantized to E4M3 with
+    per-tensor power-of-two scales (as `make_fp8`); w.q/k/v hold the exact
+    dequantized values."""
+    q_lens = [int(x) for x in q_lens]
+    k_lens = [int(x) for x in k_lens]
+    assert len(q_lens) == len(k_lens) and all(k >= q for q, k in zip(q_lens, k_lens))
+    cu = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    cu_k = np.zeros(len(k_lens) + 1, dtype=np.int32)
+    if q_lens:
+        cu[1:] = np.cumsum(np.asarray(q_lens, dtype=np.int64)).astype(np.int32)
+        cu_k[1:] = np.cumsum(np.asarray(k_lens, dtype=np.int64)).astype(np.int32)
+    T, Tk = int(cu[-1]), int(cu_k[-1])
+    qf = normal_f32(seed, STREAM_Q, (T, Hq, D))
+    kf = normal_f32(seed, STREAM_K, (Tk, Hkv, D))
+    vf = normal_f32(seed, STREAM_V, (Tk, Hkv, D))
+    (q8, sq), (k8, sk), (v8, sv) = quantize_e4m3(qf), quantize_e4m3(kf), quantize_e4m3(vf)
+    deq = lambda c, sc: f32_to_bf16_bits(e4m3_to_f32(c) * np.float32(sc))
+    sinks = normal_f32(seed, STREAM_SINKS, (Hq,), sink_sigma) if with_sinks else None
+    return Workload(name, q_lens, Hq, Hkv, D, window, scale, deq(q8, sq), deq(k8, sk),
+                    deq(v8, sv), sinks, cu, seed, cu_seqlens_k=cu_k, seqlens_k=k_lens,
+                    fp8=dict(q=q8, k=k8, v=v8, q_scale=sq, k_scale=sk, v_scale=sv))
+
+
 # The five configurations, smallest first.
 CONFIGS = {
     "tiny_1x256_h4kv1": dict(desc="1 seq x 256 tokens, Hq=4, Hkv=1, D=64, sinks N(0,1), "

@@ -174,3 +174,100 @@ def test_bench_config_sampled(name):
     print(f"{name} [{len(t)} rows]: out max {err.max():.3g} mean {err.mean():.3g} "
           f"(bound max {b.max():.3g}), lse max {np.abs(lse[t, h] - rl).max():.3g}")
     assert np.abs(lse[t, h] - rl).max() <= LSE_MAX
+
+
+def run_fp8_kvcache(w):
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    f = w.fp8
+    dev = "cuda"
+    q8, k8, v8 = (torch.from_numpy(f[n]).to(dev) for n in ("q", "k", "v"))
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    cuk = torch.from_numpy(w.cu_seqlens_k).to(dev)
+    sinks = None if w.sinks is None else torch.from_numpy(w.sinks).to(dev)
+    T = w.total_tokens
+    out = torch.full((T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((T, w.Hq), float("nan"), dtype=torch.float32, device=dev)
+    rc = pkg.tsk_mha_prefill_fp8_kvcache(q8, k8, v8, f["q_scale"], f["k_scale"], f["v_scale"],
+                                         sinks, cu, cuk, w.num_seqs, T, w.total_keys, w.Hq,
+                                         w.Hkv, w.D, w.window, w.scale, out, lse)
+    assert rc == 0, f"{pkg.STATUS.get(rc, rc)} {pkg.tsk_last_error()}"
+    torch.cuda.synchronize()
+    st = pkg.tsk_get_device_status()
+    assert st == 0, pkg.STATUS.get(st, st)
+    return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def p_rounding_bound_kvcache(w):
+    """sum_j (p_j / 256) |v_j| / l per output element over a key/value cache:
+    query i of sequence s sits at key position Lk - Lq + i."""
+    q = inputgen.bf16_bits_to_f32(w.q).astype(np.float64)
+    k = inputgen.bf16_bits_to_f32(w.k).astype(np.float64)
+    v = inputgen.bf16_bits_to_f32(w.v).astype(np.float64)
+    G = w.Hq // w.Hkv
+    bound = np.zeros(q.shape)
+    for s in range(w.num_seqs):
+        a, b = int(w.cu_seqlens[s]), int(w.cu_seqlens[s + 1])
+        ak, bk = int(w.cu_seqlens_k[s]), int(w.cu_seqlens_k[s + 1])
+        Lq, Lk = b - a, bk - ak
+        for h in range(w.Hq):
+            g = h // G
+            sc = w.scale * q[a:b, h] @ k[ak:bk, g].T           # [Lq, Lk]
+            pos = (Lk - Lq) + np.arange(Lq)[:, None]
+            j = np.arange(Lk)[None, :]
+            ok = (j <= pos) & ((j > pos - w.window) if w.window > 0 else True)
+            sc = np.where(ok, sc, -np.inf)
+            sink = w.sinks[h] if w.sinks is not None else -np.inf
+            m = np.maximum(sc.max(axis=1), sink)
+            pr = np.exp(sc - m[:, None])
+            l = pr.sum(axis=1) + np.exp(sink - m)
+            bound[a:b, h] = (np.where(ok, pr / 256, 0.0) @ np.abs(v[ak:bk, g])) / l[:, None]
+    return bound
+
+
+@pytest.mark.parametrize("q_lens,k_lens,window,D", [
+    ([1, 130, 64], [300, 130, 700], 0, 64),
+    ([200, 5], [1000, 5], 128, 64),
+    ([129, 77], [600, 300], 0, 128),
+    ([64, 1], [64, 257], 50, 128),
+])
+def test_kvcache_within_the_rounding_bound(q_lens, k_lens, window, D):
+    w = inputgen.make_kvcache_fp8(q_lens, k_lens, 8, 2, D=D, window=window,
+                                  scale=D ** -0.5, seed=sum(q_lens) + sum(k_lens) + D)
+    out, lse = run_fp8_kvcache(w)
+    ro, rl, _ = oracle.run_workload(w)
+    b = p_rounding_bound_kvcache(w)
+    label = f"kv D={D} Lq={q_lens} Lk={k_lens} W={window}"
+    err = check_within_bound(out, ro, b, label, mean_max=None)
+    print(f"{label}: out max {err.max():.3g} mean {err.mean():.3g} (bound max {b.max():.3g}), "
+          f"lse max {np.abs(lse - rl).max():.3g}")
+    assert np.abs(lse - rl).max() <= LSE_MAX
+
+
+def test_kvcache_with_equal_offsets_is_the_plain_call():
+    """cu_seqlens_k == cu_seqlens_q: bit for bit tsk_mha_prefill_fp8."""
+    import torch
+    w = inputgen.make_fp8([300, 129], 8, 2, seed=77)
+    a_out, a_lse = run_fp8(w)
+    wk = inputgen.Workload(w.name, w.seqlens, w.Hq, w.Hkv, w.D, w.window, w.scale, w.q, w.k, w.v,
+                           w.sinks, w.cu_seqlens, w.seed, cu_seqlens_k=w.cu_seqlens.copy(),
+                           seqlens_k=list(w.seqlens), fp8=w.fp8)
+    b_out, b_lse = run_fp8_kvcache(wk)
+    assert np.array_equal(a_out, b_out) and np.array_equal(a_lse, b_lse)
+
+
+def test_kvcache_bad_offsets_reported():
+    import torch
+    import gqa_attention_prefill_gb300 as pkg
+    w = inputgen.make_kvcache_fp8([100], [100], 4, 1, seed=5)
+    f = w.fp8
+    q8, k8, v8 = (torch.from_numpy(f[n]).to("cuda") for n in ("q", "k", "v"))
+    cu = torch.from_numpy(w.cu_seqlens).to("cuda")
+    out = torch.zeros((100, 4, 64), dtype=torch.bfloat16, device="cuda")
+    bad_k = torch.tensor([0, 99], dtype=torch.int32, device="cuda")   # Lk < Lq
+    args = (q8, k8, v8, f["q_scale"], f["k_scale"], f["v_scale"], None, cu, bad_k, 1, 100)
+    rc = pkg.tsk_mha_prefill_fp8_kvcache(*args, 99, 4, 1, 64, 0, 0.125, out, None)
+    assert rc == -1   # total_k < total_q is caught on the host
+    rc = pkg.tsk_mha_prefill_fp8_kvcache(*args, 100, 4, 1, 64, 0, 0.125, out, None)
+    assert rc == 0 and pkg.tsk_get_device_status() == -8
+    assert bool((out == 0).all())
