@@ -77,17 +77,6 @@ static_assert(kSmemBytesWindow <= 227 * 1024, "shared memory budget");
 
 constexpr uint32_t kColS0 = 0, kColO0 = 256, kColP0 = 384;
 constexpr uint32_t kTmemCols = 512;
-// Pooled layout of the causal kernel: three 128-column score buffers used in
-// turn by both query tiles (P overwrites the first 64 columns of its own
-// scores), then O0 and O1.
-constexpr uint32_t kPoolColO = 384;
-#ifndef TSK_POOL
-#define TSK_POOL 0
-#endif
-constexpr bool kUsePool = TSK_POOL != 0;
-#ifndef TSK_ELECT
-#define TSK_ELECT 0
-#endif
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
@@ -126,10 +115,7 @@ enum : int {
   kBarPVDone = 10 + 3 * kStages,  // [2]
   kBarDrain = 12 + 3 * kStages,  // [2] one per MMA issuer
   kBarNever = 14 + 3 * kStages,  // never signalled (stall injection)
-  kBarSPool = 15 + 3 * kStages,  // [2][3] pooled score buffers: S written, per tile and buffer
-  kBarPPool = 21 + 3 * kStages,  // [3] pooled score buffers: P written
-  kBarPVB = 24 + 3 * kStages,    // [3] pooled score buffers: PV done (buffer reusable)
-  kNumBars = 27 + 3 * kStages
+  kNumBars = 15 + 3 * kStages
 };
 static_assert(8 * kNumBars + 8 <= 512, "barrier area");
 
@@ -329,17 +315,10 @@ template <int QS>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
   bool ok = true;
-#if TSK_ELECT
-#define TSK_ISSUER_WAIT(bar, par, site) mbar_wait_warp(bar, par, site, p, cx.abort)
-#define TSK_MMA_SS(...) mma_ss_elect(__VA_ARGS__)
-#define TSK_MMA_TS(...) mma_ts_elect(__VA_ARGS__)
-#define TSK_COMMIT(bar) tc_commit_elect(bar)
-#else
 #define TSK_ISSUER_WAIT(bar, par, site) mbar_wait(bar, par, site, p, cx.abort)
 #define TSK_MMA_SS(...) mma_ss(__VA_ARGS__)
 #define TSK_MMA_TS(...) mma_ts(__VA_ARGS__)
 #define TSK_COMMIT(bar) tc_commit(bar)
-#endif
   TSK_TL_DECL;
   const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
   const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
@@ -359,11 +338,11 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
     auto issue_s = [&](int stage) {
       TSK_EV(21);
       TSK_TRACE_T0(tr_is);
-      const uint64_t dq = sdesc_sw128(qaddr);
-      const uint64_t dk = sdesc_sw128(cx.sbase + kSmemKV + stage * 2 * kTileBytes);
+      const uint32_t b = cx.sbase + kSmemKV + stage * 2 * kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        TSK_MMA_SS(d_s, dq + 2ull * kk, dk + 2ull * kk, kIdescQK, kk > 0 ? 1u : 0u);
+        TSK_MMA_SS(d_s, sdesc_sw128(qaddr + 32 * kk), sdesc_sw128(b + 32 * kk), kIdescQK,
+               kk > 0 ? 1u : 0u);
       TSK_COMMIT(cx.bar(kBarSFull + t));
       ++s_cnt;
       TSK_EV(22);
@@ -395,11 +374,12 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       if (!ok) break;
       TSK_EV(24);
       tc_fence_after();
-      const uint64_t dv = sdesc_sw128(cx.sbase + kSmemKV + sc * 2 * kTileBytes + kTileBytes);
+      const uint32_t b = cx.sbase + kSmemKV + sc * 2 * kTileBytes + kTileBytes;
       TSK_TRACE_T0(tr_ip);
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk)
-        TSK_MMA_TS(d_o, a_p + 8 * kk, dv + 128ull * kk, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        TSK_MMA_TS(d_o, a_p + 8 * kk, sdesc_sw128(b + 2048 * kk), kIdescPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
       TSK_COMMIT(cx.bar(kBarPVDone + t));
       ++p_cnt;
       TSK_EV(25);
@@ -491,128 +471,6 @@ __device__ __forceinline__ void role_mma_pair(const Ctx& cx, const AttnParams& p
   mbar_wait<true>(cx.bar(kBarDrain), 0, 14, p, cx.abort);
 }
 
-// Shared-memory operands and the QK^T instructions of the bf16 kernel (the
-// FP8 kernel has its own).
-struct Bf16Mma {
-  static __device__ __forceinline__ uint32_t q_addr(const Ctx& cx, int qb, int t) {
-    return cx.sbase + kSmemQ + (uint32_t)(2 * qb + t) * kTileBytes;
-  }
-  static __device__ __forceinline__ uint32_t k_addr(const Ctx& cx, int st) {
-    return cx.sbase + kSmemKV + (uint32_t)st * 2u * kTileBytes;
-  }
-  static __device__ __forceinline__ uint32_t v_addr(const Ctx& cx, int st) {
-    return k_addr(cx, st) + kTileBytes;
-  }
-  // (whole warp; one elected lane issues)
-  static __device__ __forceinline__ void qk(uint32_t d, uint32_t q, uint32_t k) {
-    const uint64_t dq = sdesc_sw128(q), dk = sdesc_sw128(k);
-#pragma unroll
-    for (int kk = 0; kk < kHeadDim / 16; ++kk)
-      mma_ss_elect(d, dq + 2ull * kk, dk + 2ull * kk, kIdescQK, kk > 0 ? 1u : 0u);
-  }
-};
-
-// Two tcgen05.mma issuers (whole warps; an elected lane issues) for both
-// query tiles over three pooled score buffers.  The unit's (key tile, query
-// tile) pairs are numbered in order (n = base + j * ntiles + t across the
-// CTA's units); pair n's scores go to buffer n % 3, its softmax writes P over
-// them, and PV(n) reads P from there.  Warp 1 issues every QK^T in order,
-// warp 2 every PV in order; QK^T(n) waits only for PV(n - 3), the previous
-// user of its buffer, so the scores of a tile's next key tile are computed
-// while its softmax still works on the current one, and a softmax never waits
-// for its own PV before writing P.  Barriers: SPool[t][b] (scores of tile t
-// in buffer b written; one barrier per tile and buffer, so that each has a
-// single waiter that sees all of its phases), PPool[b] (P in buffer b written,
-// four warp arrivals), PVB[b] (PV from buffer b done), PVDone[t] (PV of tile t
-// done, for the rescale of O and the epilogue).  No barrier runs more than one
-// phase ahead of its waiter: a buffer's next scores need the PV of its
-// current P.  The Q buffer of a unit is released by its last QK^T's commit and
-// by the softmax warps of both tiles once they have read it (kBarQEmpty).
-struct PoolCursor {
-  int u, j, t;
-  uint32_t q_iter, kv_iter, n;
-  Unit w;
-};
-template <int QS>
-__device__ __forceinline__ void pool_start(const Ctx& cx, const AttnParams& p, PoolCursor& c) {
-  c.u = blockIdx.x;
-  c.j = c.t = 0;
-  c.q_iter = c.kv_iter = c.n = 0;
-  if (c.u < cx.total_units) c.w = decode_unit<QS>(p, c.u);
-}
-template <int QS>
-__device__ __forceinline__ void pool_next(const Ctx& cx, const AttnParams& p, PoolCursor& c) {
-  ++c.n;
-  if (++c.t < c.w.ntiles) return;
-  c.t = 0;
-  if (++c.j < c.w.n_kv) return;
-  c.j = 0;
-  c.kv_iter += c.w.n_kv;
-  ++c.q_iter;
-  c.u += gridDim.x;
-  if (c.u < cx.total_units) c.w = decode_unit<QS>(p, c.u);
-}
-
-template <int QS, class M = Bf16Mma>
-__device__ __forceinline__ void role_mma_pool_qk(const Ctx& cx, const AttnParams& p) {
-  bool ok = true;
-  TSK_TL_DECL;
-  PoolCursor c;
-  pool_start<QS>(cx, p, c);
-  for (; ok && c.u < cx.total_units; pool_next<QS>(cx, p, c)) {
-    const int qb = c.q_iter & 1;
-    const uint32_t kv = c.kv_iter + c.j;
-    const int st = kv % kStages;
-    const uint32_t b = c.n % 3u;
-    TSK_EV(20);
-    if (c.n >= 3) ok = mbar_wait_warp(cx.bar(kBarPVB + b), ((c.n - 3u) / 3u) & 1u, 5, p, cx.abort);
-    if (ok && c.j == 0 && c.t == 0)
-      ok = mbar_wait_warp(cx.bar(kBarQFull + qb), (c.q_iter >> 1) & 1, 3, p, cx.abort);
-    if (ok && c.t == 0)
-      ok = mbar_wait_warp(cx.bar(kBarKFull + st), (kv / kStages) & 1, 6, p, cx.abort);
-    if (!ok) break;
-    TSK_EV(21);
-    tc_fence_after();
-    M::qk(cx.tmem + 128u * b, M::q_addr(cx, qb, c.t), M::k_addr(cx, st));
-    tc_commit_elect(cx.bar(kBarSPool + 3 * c.t + b));
-    if (c.j == c.w.n_kv - 1 && c.t == c.w.ntiles - 1) tc_commit_elect(cx.bar(kBarQEmpty + qb));
-    TSK_EV(22);
-  }
-  tc_commit_elect(cx.bar(kBarDrain));
-  mbar_wait<true>(cx.bar(kBarDrain), 0, 14, p, cx.abort);
-}
-
-template <int QS, class M = Bf16Mma>
-__device__ __forceinline__ void role_mma_pool_pv(const Ctx& cx, const AttnParams& p) {
-  bool ok = true;
-  TSK_TL_DECL;
-  PoolCursor c;
-  pool_start<QS>(cx, p, c);
-  for (; ok && c.u < cx.total_units; pool_next<QS>(cx, p, c)) {
-    const uint32_t kv = c.kv_iter + c.j;
-    const int st = kv % kStages;
-    const uint32_t b = c.n % 3u;
-    TSK_EV(23);
-    if (c.t == 0) ok = mbar_wait_warp(cx.bar(kBarVFull + st), (kv / kStages) & 1, 7, p, cx.abort);
-    if (ok) ok = mbar_wait_warp(cx.bar(kBarPPool + b), (c.n / 3u) & 1u, 8, p, cx.abort);
-    if (!ok) break;
-    TSK_EV(24);
-    tc_fence_after();
-    const uint64_t dv = sdesc_sw128(M::v_addr(cx, st));
-    const uint32_t d_o = cx.tmem + kPoolColO + 64u * (uint32_t)c.t;
-    const uint32_t a_p = cx.tmem + 128u * b;
-#pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk)
-      mma_ts_elect(d_o, a_p + 8 * kk, dv + 128ull * kk, kIdescPV, (c.j > 0 || kk > 0) ? 1u : 0u);
-    tc_commit_elect(cx.bar(kBarPVDone + c.t));
-    tc_commit_elect(cx.bar(kBarPVB + b));
-    if (c.t == c.w.ntiles - 1) tc_commit_elect(cx.bar(kBarKVEmpty + st));
-    TSK_EV(25);
-  }
-  tc_commit_elect(cx.bar(kBarDrain + 1));
-  mbar_wait<true>(cx.bar(kBarDrain + 1), 0, 14, p, cx.abort);
-}
-
 // Column chunks of a 128-key tile (32 keys each) classified for one warp:
 // every row of the warp sees all keys of the chunk, none of them, or some.
 struct ChunkMask {
@@ -670,7 +528,7 @@ struct Bf16Layout {
   }
 };
 
-template <int QS, class L = Bf16Layout, bool kPool = false>
+template <int QS, class L = Bf16Layout>
 __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnParams& p,
                                                     const CUtensorMap* tmO, int warp, int lane,
                                                     float out_scale = 1.f) {
@@ -679,13 +537,11 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   const int r = wq * 32 + lane;     // query row within the tile
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = cx.tmem + lane_base + kColS0 + 128 * t;
-  const uint32_t tO = cx.tmem + lane_base + (kPool ? kPoolColO : kColO0) + 64 * t;
+  const uint32_t tO = cx.tmem + lane_base + kColO0 + 64 * t;
   const uint32_t tP = cx.tmem + lane_base + kColP0 + 64 * t;
   const uint32_t epi = cx.sbase + L::kEpi + t * kTileBytes;
   const float sl2 = p.scale_log2;
   uint32_t s_cnt = 0, pv_cnt = 0, q_iter = 0;
-  uint32_t n_base = 0;  // pooled buffers: number of the unit's first (key tile, query tile) pair
-  uint32_t s_par = 0;   // pooled buffers: bit b = phase parity of this tile's next scores in buffer b
   TSK_TL_DECL;
   TSK_TRACE_T0(tr_all);
   bool ok = true;
@@ -694,16 +550,15 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   // fields are loaded before a unit's epilogue, so that their latency passes
   // while the epilogue waits for the last PV.
   struct Fields {
-    int n_kv, kv_lo, diag0, gk, nt;
+    int n_kv, kv_lo, diag0, gk;
     float sink;  // sink * log2(e), or -inf
     bool active;
   };
   auto fetch = [&](int uu) {
-    Fields f{0, 0, 0, 0, 1, -INFINITY, false};
+    Fields f{0, 0, 0, 0, -INFINITY, false};
     if (uu < cx.total_units) {
       const Unit w = decode_unit<QS>(p, uu);
       f.active = t < w.ntiles;
-      f.nt = w.ntiles;
       f.gk = w.g;
       f.n_kv = w.n_kv;
       f.kv_lo = w.kv_lo;
@@ -723,38 +578,24 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     ++q_iter;
     const Fields cf = nx;
     if (!cf.active) {
-      if constexpr (kPool) {
-        // (every softmax warp takes part in every unit's Q buffer handover)
-        ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qb));
-      }
-      n_base += (uint32_t)(cf.nt * cf.n_kv);
       nx = fetch(u + gridDim.x);
       continue;
     }
-    const int n_kv = cf.n_kv, kv_lo = cf.kv_lo, diag0 = cf.diag0, gk = cf.gk, nt = cf.nt;
+    const int n_kv = cf.n_kv, kv_lo = cf.kv_lo, diag0 = cf.diag0, gk = cf.gk;
     const int pos = diag0 + r;  // key position of this thread's query row
     float m_used = cf.sink, l = cf.sink == -INFINITY ? 0.f : 1.f;
     TSK_TRACE_ADD(24, tr_dec);
     // Bound on x = s * scale * log2(e) for every key of this row: ||q|| times
     // the largest key norm of the KV head (Cauchy-Schwarz).
     float bq = INFINITY;
-    if (kPool || p.knorm) {
+    if (p.knorm) {
       TSK_EV(16);
       ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
       if (!ok) break;
       TSK_EV(18);
-    }
-    if (p.knorm) {
       const float sq = L::q_sq(cx.sbase + L::kQ + (2 * qb + t) * L::kQTile, r);
       bq = sl2 * sqrtf(sq) * ld_shared_f32(cx.sbase + L::kNorm + 4u * (uint32_t)gk);
       TSK_EV(19);
-    }
-    if constexpr (kPool) {
-      // (with the pooled issuer the Q buffer waits for this warp's arrival)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qb));
     }
     // One key tile.  A slow tile computes its row maximum and raises the
     // maximum in use, m_used, when the tile exceeds it by more than
@@ -766,34 +607,21 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       constexpr bool kSlow = decltype(slow_tag)::value;
       const int kt = kv_lo + j;
       TSK_EV(1);
-      uint32_t tSj = tS, bj = 0;  // this key tile's score buffer (and its pool index)
-      if constexpr (kPool) {
-        const uint32_t n = n_base + (uint32_t)(j * nt + t);
-        bj = n % 3u;
-        tSj = cx.tmem + lane_base + 128u * bj;
-        if (!mbar_wait_warp(cx.bar(kBarSPool + 3 * t + bj), (s_par >> bj) & 1u, j == 0 ? 26 : 9,
-                            p, cx.abort))
-          return false;
-        s_par ^= 1u << bj;
-      } else {
-        if (!mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort))
-          return false;
-        ++s_cnt;
-      }
+      if (!mbar_wait_warp(cx.bar(kBarSFull + t), s_cnt & 1, j == 0 ? 26 : 9, p, cx.abort))
+        return false;
       TSK_EV(2);
+      ++s_cnt;
       tc_fence_after();
       TSK_TRACE_T0(tr_ld);
       uint32_t sr[128];
-      tmem_ld_32x32b_x128(tSj, sr);  // (one 128-column load: fewer instructions than four)
+      tmem_ld_32x32b_x128(tS, sr);  // (one 128-column load: fewer instructions than four)
       tmem_wait_ld();
       reg_fence<128>(sr);
       TSK_TRACE_ADD(20, tr_ld);
       TSK_EV(3);
-      if constexpr (!kPool) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(kBarSFree + t));
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -880,11 +708,8 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       }
       TSK_TRACE_ADD(22, tr_exp);
       TSK_EV(5);
-      // (pooled buffers: P overwrites this tile's scores, which nothing else reads)
-      if constexpr (kPool) tmem_st_32x32b_x64(tSj, pk);
       if (j > 0) {
-        // O_t is stable (and, without the pool, P_t reusable) once PV_t(j-1)
-        // has completed.
+        // O_t is stable and P_t reusable once PV_t(j-1) has completed.
         if (!mbar_wait_warp(cx.bar(kBarPVDone + t), pv_cnt & 1, 10, p, cx.abort)) return false;
         TSK_EV(6);
         ++pv_cnt;
@@ -902,12 +727,12 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
         }
       }
       TSK_TRACE_T0(tr_st);
-      if constexpr (!kPool) tmem_st_32x32b_x64(tP, pk);
+      tmem_st_32x32b_x64(tP, pk);
       tmem_wait_st();
       TSK_TRACE_ADD(23, tr_st);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(kPool ? kBarPPool + bj : kBarPFull + t));
+      if (lane == 0) mbar_arrive(cx.bar(kBarPFull + t));
       TSK_EV(7);
       return true;
     };
@@ -920,7 +745,6 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     }
     for (; j < n_kv && ok; ++j) ok = step(j, FastTile{});
     if (!ok) break;
-    n_base += (uint32_t)(nt * n_kv);
     nx = fetch(u + gridDim.x);
     // ------------------------------------------------------------ epilogue
     TSK_EV(9);
@@ -1283,10 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(cx.bar(kBarQFull + i), 1);
-      // one issuer, or one per tile; the pooled issuer's commit plus the
-      // arrivals of the softmax warps of both tiles
-      mbar_init(cx.bar(kBarQEmpty + i),
-                kSmallWindow ? 1 : kUsePool ? 1 + 2 * kSoftmaxWarpsPerTile : 2);
+      mbar_init(cx.bar(kBarQEmpty + i), kSmallWindow ? 1 : 2);  // (one issuer, or one per tile)
       mbar_init(cx.bar(kBarSFull + i), 1);
       mbar_init(cx.bar(kBarSFree + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPFull + i), kSoftmaxWarpsPerTile);
@@ -1295,13 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(cx.bar(kBarKFull + s), 1);
       mbar_init(cx.bar(kBarVFull + s), 1);
-      mbar_init(cx.bar(kBarKVEmpty + s), (kSmallWindow || kUsePool) ? 1 : 2);
-    }
-    for (int b = 0; b < 3; ++b) {
-      mbar_init(cx.bar(kBarSPool + b), 1);
-      mbar_init(cx.bar(kBarSPool + 3 + b), 1);
-      mbar_init(cx.bar(kBarPPool + b), kSoftmaxWarpsPerTile);
-      mbar_init(cx.bar(kBarPVB + b), 1);
+      mbar_init(cx.bar(kBarKVEmpty + s), kSmallWindow ? 1 : 2);
     }
     mbar_init(cx.bar(kBarDrain), 1);
     mbar_init(cx.bar(kBarDrain + 1), 1);
@@ -1335,13 +1150,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) role_producer<QS>(cx, &tmQ, &tmK, &tmV, p);
   else if (kSmallWindow && warp == 1 && lane == 0) role_mma_pair<QS>(cx, p);
-  else if (!kSmallWindow && kUsePool && warp == 1) role_mma_pool_qk<QS>(cx, p);
-  else if (!kSmallWindow && kUsePool && warp == 2) role_mma_pool_pv<QS>(cx, p);
-  else if (!kSmallWindow && !kUsePool && warp == 1 && (TSK_ELECT || lane == 0)) role_mma<QS>(cx, p, 0);
-  else if (!kSmallWindow && !kUsePool && warp == 2 && (TSK_ELECT || lane == 0)) role_mma<QS>(cx, p, 1);
+  else if (!kSmallWindow && warp == 1 && lane == 0) role_mma<QS>(cx, p, 0);
+  else if (!kSmallWindow && warp == 2 && lane == 0) role_mma<QS>(cx, p, 1);
   else if (warp >= kFirstSoftmaxWarp) {
     if constexpr (kSmallWindow) role_softmax_window<QS>(cx, p, &tmO, warp, lane);
-    else role_softmax_causal<QS, Bf16Layout, kUsePool>(cx, p, &tmO, warp, lane);
+    else role_softmax_causal<QS>(cx, p, &tmO, warp, lane);
   }
 
   // ------------------------------------------------------------------ teardown
