@@ -309,8 +309,10 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
 //   S_t(j+1) = Q_t K_{j+1}^T   once K_{j+1} is loaded and the softmax has read S_t(j)
 //   O_t += P_t(j) V_j          once V_j is loaded and the softmax has written P_t(j)
 // Each issuer releases a K/V stage (and the Q buffer) with its own commit, so
-// those barriers count two arrivals; for a unit with one query tile the tile-0
-// issuer commits twice and the tile-1 issuer only advances its counters.
+// those barriers count two arrivals (the Q buffer also counts the eight softmax
+// warps); in a unit with one query tile the tile-1 issuer still waits for each
+// of the unit's fills and releases it with a plain arrival, so that no fill is
+// replaced before both issuers have seen it.
 template <int QS>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, s_cnt = 0, p_cnt = 0;
@@ -326,14 +328,26 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit<QS>(p, u);
     const int qb = q_iter & 1;
-    if (t >= w.ntiles) {  // this tile is idle in the unit
+    ok = TSK_ISSUER_WAIT(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3);
+    if (!ok) break;
+    if (t >= w.ntiles) {
+      // This tile is idle in the unit: follow the unit's K/V fills and release
+      // them (and the Q buffer) like a present tile, so that no fill can be
+      // replaced before this thread has seen it (no barrier ever runs two
+      // phases ahead of it).
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        const uint32_t cur = kv_iter + j;
+        const int sc = cur % kStages;
+        ok = TSK_ISSUER_WAIT(cx.bar(kBarKFull + sc), (cur / kStages) & 1, 4);
+        if (ok) ok = TSK_ISSUER_WAIT(cx.bar(kBarVFull + sc), (cur / kStages) & 1, 7);
+        if (ok) mbar_arrive(cx.bar(kBarKVEmpty + sc));
+      }
+      if (!ok) break;
+      mbar_arrive(cx.bar(kBarQEmpty + qb));
       kv_iter += w.n_kv;
       ++q_iter;
       continue;
     }
-    const int commits = w.ntiles == 1 ? 2 : 1;  // arrivals owed on the shared release barriers
-    ok = TSK_ISSUER_WAIT(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3);
-    if (!ok) break;
     const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kTileBytes;
     auto issue_s = [&](int stage) {
       TSK_EV(21);
@@ -384,11 +398,11 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
       ++p_cnt;
       TSK_EV(25);
       TSK_TRACE_ADD(16, tr_ip);
-      for (int c = 0; c < commits; ++c) TSK_COMMIT(cx.bar(kBarKVEmpty + sc));
+      TSK_COMMIT(cx.bar(kBarKVEmpty + sc));
     }
     if (!ok) break;
     kv_iter += w.n_kv;
-    for (int c = 0; c < commits; ++c) TSK_COMMIT(cx.bar(kBarQEmpty + qb));
+    TSK_COMMIT(cx.bar(kBarQEmpty + qb));
     ++q_iter;
   }
   // Make sure none of this thread's MMAs is still running before TMEM is freed.
@@ -577,6 +591,16 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     const uint32_t q_par = (q_iter >> 1) & 1;
     ++q_iter;
     const Fields cf = nx;
+    // Every softmax warp takes part in every unit's Q buffer handover (the
+    // release counts both issuers and all eight softmax warps), so that no
+    // warp can fall two phases behind the Q barriers: a present tile with the
+    // key-norm bound arrives once it has read its query rows, the others here.
+    if (!cf.active || !p.knorm) {
+      ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qb));
+    }
     if (!cf.active) {
       nx = fetch(u + gridDim.x);
       continue;
@@ -596,6 +620,8 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
       const float sq = L::q_sq(cx.sbase + L::kQ + (2 * qb + t) * L::kQTile, r);
       bq = sl2 * sqrtf(sq) * ld_shared_f32(cx.sbase + L::kNorm + 4u * (uint32_t)gk);
       TSK_EV(19);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qb));
     }
     // One key tile.  A slow tile computes its row maximum and raises the
     // maximum in use, m_used, when the tile exceeds it by more than
@@ -1107,7 +1133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(cx.bar(kBarQFull + i), 1);
-      mbar_init(cx.bar(kBarQEmpty + i), kSmallWindow ? 1 : 2);  // (one issuer, or one per tile)
+      // one issuer; or one per tile plus the eight softmax warps
+      mbar_init(cx.bar(kBarQEmpty + i), kSmallWindow ? 1 : 2 + 2 * kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarSFull + i), 1);
       mbar_init(cx.bar(kBarSFree + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPFull + i), kSoftmaxWarpsPerTile);

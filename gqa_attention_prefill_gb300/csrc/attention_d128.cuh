@@ -164,8 +164,8 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
 }
 
 // tcgen05.mma issuer for query tile t (one thread).  The release barriers
-// (Q, K and V buffers) count one arrival per tile; for a unit with a single
-// query tile, tile 0 arrives twice.
+// (Q, K and V buffers) count one arrival per tile; in a unit with a single
+// query tile the tile-1 issuer follows the fills and arrives without MMAs.
 template <int QS, bool kFp8>
 __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int t) {
   uint32_t q_iter = 0, kv_iter = 0, p_cnt = 0;
@@ -178,14 +178,25 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit<QS>(p, u);
     if (t >= w.ntiles) {
+      // Idle in the unit: follow its Q and K/V fills and release them with
+      // plain arrivals, so that no fill is replaced before both issuers have
+      // seen it (no barrier runs two phases ahead of this thread).
+      ok = mbar_wait(cx.bar(kBarQFull), q_iter & 1, 3, p, cx.abort);
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        const uint32_t cur = kv_iter + j;
+        const int sc = cur % kStagesKV;
+        ok = mbar_wait(cx.bar(kBarKFull + sc), (cur / kStagesKV) & 1, 4, p, cx.abort);
+        if (ok) mbar_arrive(cx.bar(kBarKEmpty + sc));
+        if (ok) ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStagesKV) & 1, 7, p, cx.abort);
+        if (ok) mbar_arrive(cx.bar(kBarVEmpty + sc));
+      }
+      if (!ok) break;
+      mbar_arrive(cx.bar(kBarQEmpty));
       kv_iter += w.n_kv;
       ++q_iter;
       continue;
     }
-    const int commits = w.ntiles == 1 ? 2 : 1;
-    auto release = [&](int bar) {
-      for (int c = 0; c < commits; ++c) tc_commit(cx.bar(bar));
-    };
+    auto release = [&](int bar) { tc_commit(cx.bar(bar)); };
     auto issue_qk = [&](uint32_t it) {
       const int s = it % kStagesKV;
       const uint32_t kb = cx.sbase + kSmemKV + s * 2 * kTile;

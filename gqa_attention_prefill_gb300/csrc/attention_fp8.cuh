@@ -219,14 +219,23 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     const int qb = q_iter & 1;
+    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3, p, cx.abort);
+    if (!ok) break;
     if (t >= w.ntiles) {
+      // idle in the unit: follow and release its K/V fills and its Q buffer
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        const uint32_t cur = kv_iter + j;
+        const int sc = cur % kStages;
+        ok = mbar_wait(cx.bar(kBarKFull + sc), (cur / kStages) & 1, 4, p, cx.abort);
+        if (ok) ok = mbar_wait(cx.bar(kBarVFull + sc), (cur / kStages) & 1, 7, p, cx.abort);
+        if (ok) mbar_arrive(cx.bar(kBarKVEmpty + sc));
+      }
+      if (!ok) break;
+      mbar_arrive(cx.bar(kBarQEmpty + qb));
       kv_iter += w.n_kv;
       ++q_iter;
       continue;
     }
-    const int commits = w.ntiles == 1 ? 2 : 1;
-    ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3, p, cx.abort);
-    if (!ok) break;
     const uint32_t qaddr = cx.sbase + kSmemQ + (2 * qb + t) * kQTile;
     auto issue_s = [&](int stage) {
       const uint32_t b = cx.sbase + kSmemKV + stage * kStageBytes;
@@ -267,11 +276,11 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
                (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(cx.bar(kBarPVDone + t));
       ++p_cnt;
-      for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarKVEmpty + sc));
+      tc_commit(cx.bar(kBarKVEmpty + sc));
     }
     if (!ok) break;
     kv_iter += w.n_kv;
-    for (int c = 0; c < commits; ++c) tc_commit(cx.bar(kBarQEmpty + qb));
+    tc_commit(cx.bar(kBarQEmpty + qb));
     ++q_iter;
   }
   tc_commit(cx.bar(kBarDrain + t));
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(cx.bar(kBarQFull + i), 1);
-      mbar_init(cx.bar(kBarQEmpty + i), 2);
+      mbar_init(cx.bar(kBarQEmpty + i), 2 + 2 * kSoftmaxWarpsPerTile);  // issuers and softmax warps
       mbar_init(cx.bar(kBarSFull + i), 1);
       mbar_init(cx.bar(kBarSFree + i), kSoftmaxWarpsPerTile);
       mbar_init(cx.bar(kBarPFull + i), kSoftmaxWarpsPerTile);
