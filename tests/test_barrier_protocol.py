@@ -1,0 +1,218 @@
+"""A model of the causal D = 64 kernel's mbarrier protocol, run with random
+timing on the CPU.
+
+The roles of one CTA (TMA producer, the two tiles' MMA issuers, the two
+tiles' softmax warpgroups) are generators that wait on parity barriers and
+arrive on them exactly as in attention.cuh: a Q double buffer (release: one
+commit per issuer plus the eight softmax warps), a ring of three K/V stages
+(release: one commit per issuer), per-tile S, S-free, P and PV barriers.
+Copies and MMAs complete at random later times; each issuer's MMAs complete
+in issue order.  Every wait that passes is checked to have seen exactly the
+phase it waits for: a barrier two phases ahead of its waiter would pass a
+parity wait for the wrong phase.  Units mix one and two query tiles (odd
+group sizes; the last row block of a sequence with one query head per KV
+head) and one to five key tiles.
+
+The same model with the earlier rule for a unit with one query tile (the
+idle tile's issuer skips the unit and the present tile's issuer releases
+twice) is shown to fail: the check finds the aliasing it allowed."""
+import random
+
+import pytest
+
+K_STAGES = 3
+
+
+class Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.phase = count, 0, 0
+
+    def arrive(self, n=1):
+        self.pending += n
+        assert self.pending <= self.count, "more arrivals than the count"
+        if self.pending == self.count:
+            self.phase += 1
+            self.pending = 0
+
+    def passes(self, parity):
+        return (self.phase & 1) != parity
+
+
+class Aliasing(AssertionError):
+    pass
+
+
+class Deadlock(AssertionError):
+    pass
+
+
+def run_model(units, seed, idle_follows=True):
+    """units: list of (ntiles, n_kv).  Raises Deadlock or Aliasing."""
+    rnd = random.Random(seed)
+    bars = {}
+
+    def bar(name, count):
+        bars[name] = Bar(count)
+
+    for i in range(2):
+        bar(("QFull", i), 1)
+        bar(("QEmpty", i), 2 + (8 if idle_follows else 0))
+    for s in range(K_STAGES):
+        bar(("KFull", s), 1)
+        bar(("VFull", s), 1)
+        bar(("KVEmpty", s), 2)
+    for t in range(2):
+        for name, count in (("SFull", 1), ("SFree", 4), ("PFull", 4), ("PVDone", 1)):
+            bar((name, t), count)
+    copies = []            # pending TMA completions
+    pipes = {0: [], 1: []}  # each issuer's MMAs/commits, completed in order
+
+    def wait(name, index):
+        """Wait for completion of phase `index` of barrier `name`."""
+        return ("wait", name, index)
+
+    def producer():
+        q_iter = kv_iter = 0
+        for nt, nkv in units:
+            qb = q_iter & 1
+            if q_iter >= 2:
+                yield wait(("QEmpty", qb), (q_iter >> 1) - 1)
+            copies.append(lambda qb=qb: bars[("QFull", qb)].arrive())
+            q_iter += 1
+            for _ in range(nkv):
+                st = kv_iter % K_STAGES
+                if kv_iter >= K_STAGES:
+                    yield wait(("KVEmpty", st), kv_iter // K_STAGES - 1)
+                copies.append(lambda st=st: bars[("KFull", st)].arrive())
+                copies.append(lambda st=st: bars[("VFull", st)].arrive())
+                kv_iter += 1
+
+    def issuer(t):
+        q_iter = kv_iter = s_cnt = p_cnt = 0
+        pipe = pipes[t]
+        for nt, nkv in units:
+            qb = q_iter & 1
+            if t >= nt:
+                if idle_follows:
+                    yield wait(("QFull", qb), q_iter >> 1)
+                    for j in range(nkv):
+                        cur = kv_iter + j
+                        yield wait(("KFull", cur % K_STAGES), cur // K_STAGES)
+                        yield wait(("VFull", cur % K_STAGES), cur // K_STAGES)
+                        bars[("KVEmpty", cur % K_STAGES)].arrive()
+                    bars[("QEmpty", qb)].arrive()
+                kv_iter += nkv
+                q_iter += 1
+                continue
+            releases = 2 if (nt == 1 and not idle_follows) else 1
+            yield wait(("QFull", qb), q_iter >> 1)
+            yield wait(("KFull", kv_iter % K_STAGES), kv_iter // K_STAGES)
+            if s_cnt > 0:
+                yield wait(("SFree", t), s_cnt - 1)
+            pipe.append(("SFull", t))
+            s_cnt += 1
+            for j in range(nkv):
+                cur = kv_iter + j
+                if j + 1 < nkv:
+                    yield wait(("KFull", (cur + 1) % K_STAGES), (cur + 1) // K_STAGES)
+                    yield wait(("SFree", t), s_cnt - 1)
+                    pipe.append(("SFull", t))
+                    s_cnt += 1
+                yield wait(("VFull", cur % K_STAGES), cur // K_STAGES)
+                yield wait(("PFull", t), p_cnt)
+                p_cnt += 1
+                pipe.append(("PVDone", t))
+                pipe.extend([("KVEmpty", cur % K_STAGES)] * releases)
+            kv_iter += nkv
+            pipe.extend([("QEmpty", qb)] * releases)
+            q_iter += 1
+
+    def softmax(t):
+        s_cnt = pv_cnt = q_iter = 0
+        for nt, nkv in units:
+            qb = q_iter & 1
+            q_index = q_iter >> 1
+            q_iter += 1
+            if t >= nt and not idle_follows:
+                continue
+            yield wait(("QFull", qb), q_index)  # (the key-norm bound reads Q)
+            if idle_follows:
+                bars[("QEmpty", qb)].arrive(4)
+            if t >= nt:
+                continue
+            for j in range(nkv):
+                yield wait(("SFull", t), s_cnt)
+                s_cnt += 1
+                bars[("SFree", t)].arrive(4)
+                yield ("step",)
+                if j > 0:
+                    yield wait(("PVDone", t), pv_cnt)
+                    pv_cnt += 1
+                bars[("PFull", t)].arrive(4)
+            yield wait(("PVDone", t), pv_cnt)  # the epilogue's wait for the last PV
+            pv_cnt += 1
+
+    roles = {"producer": producer(), "mma0": issuer(0), "mma1": issuer(1),
+             "softmax0": softmax(0), "softmax1": softmax(1)}
+    blocked = dict.fromkeys(roles)
+    done = set()
+    while len(done) < len(roles):
+        ready = [k for k in roles if k not in done and
+                 (blocked[k] is None or bars[blocked[k][0]].passes(blocked[k][1] & 1))]
+        choices = [("role", k) for k in ready]
+        choices += [("copy", None)] if copies else []
+        choices += [("mma", t) for t in (0, 1) if pipes[t]]
+        if not choices:
+            raise Deadlock(f"blocked: {blocked}")
+        kind, k = rnd.choice(choices)
+        if kind == "copy":
+            copies.pop(rnd.randrange(len(copies)))()
+            continue
+        if kind == "mma":
+            bars[pipes[k].pop(0)].arrive()
+            continue
+        if blocked[k] is not None:
+            name, index = blocked[k]
+            if bars[name].phase != index + 1:
+                raise Aliasing(f"{k} passed a wait for phase {index} of {name} "
+                               f"at {bars[name].phase} completed phases")
+            blocked[k] = None
+        try:
+            while True:
+                action = next(roles[k])
+                if action[0] != "wait":
+                    break
+                _, name, index = action
+                if not bars[name].passes(index & 1):
+                    blocked[k] = (name, index)
+                    break
+                if bars[name].phase != index + 1:
+                    raise Aliasing(f"{k} passed a wait for phase {index} of {name} "
+                                   f"at {bars[name].phase} completed phases")
+        except StopIteration:
+            done.add(k)
+
+
+def random_units(rnd, mixed=True):
+    return [(rnd.choice([1, 2, 2, 2] if mixed else [2]), rnd.choice([1, 1, 2, 3, 5]))
+            for _ in range(rnd.randint(1, 9))]
+
+
+@pytest.mark.parametrize("mixed", [False, True])
+def test_protocol_never_deadlocks_or_aliases(mixed):
+    rnd = random.Random(1234 + mixed)
+    for trial in range(1500):
+        run_model(random_units(rnd, mixed), seed=trial)
+
+
+def test_skipping_idle_tiles_can_alias():
+    """The earlier rule fails the same check for some timing: the check has
+    the power to find this class of hazard."""
+    rnd = random.Random(99)
+    failures = 0
+    for trial in range(3000):
+        try:
+            run_model(random_units(rnd, True), seed=trial, idle_follows=False)
+        except (Aliasing, Deadlock):
+            failures += 1
+    assert failures > 0
