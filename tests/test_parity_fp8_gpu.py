@@ -176,6 +176,22 @@ def test_bench_config_sampled(name):
     assert np.abs(lse[t, h] - rl).max() <= LSE_MAX
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_odd_group_mixes_one_and_two_tile_units(D):
+    """G = 5: the CTAs alternate units with one and two query tiles (see the
+    bf16 test of the same name)."""
+    w = inputgen.make_fp8([1536, 2000, 700, 129], 40, 8, D=D, scale=D ** -0.5, seed=50 + D)
+    out, lse = run_fp8(w)
+    t, h = inputgen.sample_rows(w, n_target=4096)
+    ro, rl, _ = oracle.mha_prefill_rows(w.q, w.k, w.v, w.sinks, w.cu_seqlens, w.Hq, w.Hkv, w.D,
+                                        w.window, w.scale, t, h)
+    assert np.isfinite(out).all()
+    b = p_rounding_bound_rows(w, t, h)
+    err = check_within_bound(out[t, h], ro, b, f"G=5 D={D} [{len(t)} rows]")
+    print(f"G=5 D={D}: out max {err.max():.3g} mean {err.mean():.3g}")
+    assert np.abs(lse[t, h] - rl).max() <= LSE_MAX
+
+
 def run_fp8_kvcache(w):
     import torch
     import gqa_attention_prefill_gb300 as pkg

@@ -41,6 +41,18 @@ def test_head_groupings(Hq, Hkv):
     print(parity.check_full(w, label=f"Hq={Hq},Hkv={Hkv}"))
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("window", [0, 700])
+def test_odd_group_mixes_one_and_two_tile_units(D, window):
+    """G = 5: every KV head has two head pairs and one single head, and with
+    the CTAs' stride over the units (152 = 2 mod 3) each CTA alternates units
+    with one and two query tiles, so the idle tile's issuer and softmax warps
+    follow and release fills between present units many times per CTA."""
+    w = inputgen.make([1536, 2000, 700, 129], 40, 8, D=D, window=window,
+                      scale=D ** -0.5, seed=D + window)
+    print(parity.check_sampled(w, n_rows=8192, label=f"G=5 D={D} W={window}"))
+
+
 def test_no_sinks_and_no_lse():
     w = inputgen.make([130, 257], 8, 2, window=0, seed=4, with_sinks=False)
     print(parity.check_full(w, label="no sinks"))
