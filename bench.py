@@ -222,6 +222,10 @@ def roofline_of(flops, alg_bytes, kernel_s, peaks, peak_src, fp8=False):
     roofs = {
         "tensor": {"achieved": flops / kernel_s / 1e12, "peak": tensor_peak, "unit": "TFLOP/s",
                    "frac": flops / kernel_s / 1e12 / tensor_peak,
+                   # (the same against the peak measured over a seconds-long loop
+                   # under the power cap)
+                   "frac_of_sustained": flops / kernel_s / 1e12 /
+                                        (peaks["bf16_tflops_sustained"] * (4.0 / 3.0 if fp8 else 1.0)),
                    "peak_source": (f"{peak_src} dense bf16 (burst) x 4/3 (E4M3 QK^T at 2x, "
                                    "bf16 PV)" if fp8 else f"{peak_src} dense bf16 (burst)")},
         "hbm": {"achieved": alg_bytes / kernel_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -503,6 +507,7 @@ def main():
         "config": config_dict(w, ws),
         "tokens_per_s": T * ws / (ms * 1e-3),
         "pct_of_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
+        "pct_of_bf16_sustained_peak": value / peaks["bf16_tflops_sustained"] * 100.0,
         "unmasked_flop_per_step": flops,
         "attention_kernel_ms": attn_avg, "prepass_kernel_ms": sum(pre_ms) / len(pre_ms),
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
