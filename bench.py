@@ -285,7 +285,9 @@ def run_reference(args, ws, rank):
     value = statistics.median(rates) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
-        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        # (the launch's GPU count, as in the GPU arm's line; the oracle itself
+        # runs on the host's cores, see cpu_baseline)
+        "n_gpus": ws, "runs_on": "host CPU cores", "steps": args.steps, "warmup": args.warmup,
         # measured wall time of one step (a bounded row sample, rate calibration included)
         "ms_per_step": statistics.mean(step_s) * 1e3,
         "higher_is_better": True, "scaling": "weak",
