@@ -566,10 +566,11 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
   struct Fields {
     int n_kv, kv_lo, diag0, gk;
     float sink;  // sink * log2(e), or -inf
+    float bq;    // bound on the row's scores (key-norm bound), or +inf
     bool active;
   };
   auto fetch = [&](int uu) {
-    Fields f{0, 0, 0, 0, -INFINITY, false};
+    Fields f{0, 0, 0, 0, -INFINITY, INFINITY, false};
     if (uu < cx.total_units) {
       const Unit w = decode_unit<QS>(p, uu);
       f.active = t < w.ntiles;
@@ -583,46 +584,45 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     }
     return f;
   };
+  // Q buffer handover of unit uu (the qi-th unit of this CTA): every softmax
+  // warp takes part in every unit's (the release counts both issuers and all
+  // eight softmax warps), so that no warp can fall two phases behind the Q
+  // barriers.  A present tile reads its query rows first, for the bound on
+  // x = s * scale * log2(e) over every key of a row: ||q|| times the largest
+  // key norm of the KV head (Cauchy-Schwarz).  Done for the next unit before
+  // a unit's epilogue, so that it overlaps the wait for the last PV.
+  auto handover = [&](int uu, uint32_t qi, Fields& f) -> bool {
+    if (uu >= cx.total_units) return true;
+    const int qbb = qi & 1;
+    TSK_EV(16);
+    if (!mbar_wait_warp(cx.bar(kBarQFull + qbb), (qi >> 1) & 1, 17, p, cx.abort)) return false;
+    TSK_EV(18);
+    if (f.active && p.knorm) {
+      const float sq = L::q_sq(cx.sbase + L::kQ + (2 * qbb + t) * L::kQTile, r);
+      f.bq = sl2 * sqrtf(sq) * ld_shared_f32(cx.sbase + L::kNorm + 4u * (uint32_t)f.gk);
+    }
+    TSK_EV(19);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qbb));
+    return true;
+  };
   Fields nx = fetch(blockIdx.x);
+  ok = handover(blockIdx.x, 0, nx);
   for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
     TSK_EV(8);
     TSK_TRACE_T0(tr_dec);
-    const int qb = q_iter & 1;
-    const uint32_t q_par = (q_iter >> 1) & 1;
-    ++q_iter;
+    ++q_iter;  // (now the next unit's index)
     const Fields cf = nx;
-    // Every softmax warp takes part in every unit's Q buffer handover (the
-    // release counts both issuers and all eight softmax warps), so that no
-    // warp can fall two phases behind the Q barriers: a present tile with the
-    // key-norm bound arrives once it has read its query rows, the others here.
-    if (!cf.active || !p.knorm) {
-      ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
-      if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qb));
-    }
     if (!cf.active) {
       nx = fetch(u + gridDim.x);
+      ok = handover(u + gridDim.x, q_iter, nx);
       continue;
     }
-    const int n_kv = cf.n_kv, kv_lo = cf.kv_lo, diag0 = cf.diag0, gk = cf.gk;
+    const int n_kv = cf.n_kv, kv_lo = cf.kv_lo, diag0 = cf.diag0;
     const int pos = diag0 + r;  // key position of this thread's query row
     float m_used = cf.sink, l = cf.sink == -INFINITY ? 0.f : 1.f;
     TSK_TRACE_ADD(24, tr_dec);
-    // Bound on x = s * scale * log2(e) for every key of this row: ||q|| times
-    // the largest key norm of the KV head (Cauchy-Schwarz).
-    float bq = INFINITY;
-    if (p.knorm) {
-      TSK_EV(16);
-      ok = mbar_wait_warp(cx.bar(kBarQFull + qb), q_par, 17, p, cx.abort);
-      if (!ok) break;
-      TSK_EV(18);
-      const float sq = L::q_sq(cx.sbase + L::kQ + (2 * qb + t) * L::kQTile, r);
-      bq = sl2 * sqrtf(sq) * ld_shared_f32(cx.sbase + L::kNorm + 4u * (uint32_t)gk);
-      TSK_EV(19);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(kBarQEmpty + qb));
-    }
+    const float bq = cf.bq;
     // One key tile.  A slow tile computes its row maximum and raises the
     // maximum in use, m_used, when the tile exceeds it by more than
     // kRescaleThreshold (p <= 2^8 then).  A fast tile skips the maximum and
@@ -772,6 +772,8 @@ __device__ __forceinline__ void role_softmax_causal(const Ctx& cx, const AttnPar
     for (; j < n_kv && ok; ++j) ok = step(j, FastTile{});
     if (!ok) break;
     nx = fetch(u + gridDim.x);
+    ok = handover(u + gridDim.x, q_iter, nx);
+    if (!ok) break;
     // ------------------------------------------------------------ epilogue
     TSK_EV(9);
     const int per_tile = p.Hkv * p.HP;

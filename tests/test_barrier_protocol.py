@@ -128,29 +128,37 @@ def run_model(units, seed, idle_follows=True):
             q_iter += 1
 
     def softmax(t):
-        s_cnt = pv_cnt = q_iter = 0
-        for nt, nkv in units:
-            qb = q_iter & 1
-            q_index = q_iter >> 1
-            q_iter += 1
-            if t >= nt and not idle_follows:
-                continue
-            yield wait(("QFull", qb), q_index)  # (the key-norm bound reads Q)
+        s_cnt = pv_cnt = 0
+
+        def handover(i):
+            # the Q handover of unit i: taken before unit i - 1's epilogue (the
+            # key-norm bound reads Q); the earlier rule took it only in units
+            # with this tile present, at their start
+            nt_i = units[i][0]
+            if not idle_follows and t >= nt_i:
+                return
+            yield wait(("QFull", i & 1), i >> 1)
             if idle_follows:
-                bars[("QEmpty", qb)].arrive(4)
-            if t >= nt:
-                continue
-            for j in range(nkv):
-                yield wait(("SFull", t), s_cnt)
-                s_cnt += 1
-                bars[("SFree", t)].arrive(4)
-                yield ("step",)
-                if j > 0:
-                    yield wait(("PVDone", t), pv_cnt)
-                    pv_cnt += 1
-                bars[("PFull", t)].arrive(4)
-            yield wait(("PVDone", t), pv_cnt)  # the epilogue's wait for the last PV
-            pv_cnt += 1
+                bars[("QEmpty", i & 1)].arrive(4)
+
+        if units:
+            yield from handover(0)
+        for i, (nt, nkv) in enumerate(units):
+            if t < nt:
+                for j in range(nkv):
+                    yield wait(("SFull", t), s_cnt)
+                    s_cnt += 1
+                    bars[("SFree", t)].arrive(4)
+                    yield ("step",)
+                    if j > 0:
+                        yield wait(("PVDone", t), pv_cnt)
+                        pv_cnt += 1
+                    bars[("PFull", t)].arrive(4)
+            if i + 1 < len(units):
+                yield from handover(i + 1)
+            if t < nt:
+                yield wait(("PVDone", t), pv_cnt)  # the epilogue's wait for the last PV
+                pv_cnt += 1
 
     roles = {"producer": producer(), "mma0": issuer(0), "mma1": issuer(1),
              "softmax0": softmax(0), "softmax1": softmax(1)}
