@@ -53,44 +53,65 @@ def test_odd_group_mixes_one_and_two_tile_units(D, window):
     print(parity.check_sampled(w, n_rows=8192, label=f"G=5 D={D} W={window}"))
 
 
+def few_key_rounding_bound(w):
+    """sum_j (p_j / 256)|v_j| / l per output element for a window of a few
+    keys (the bf16 rounding of P, relative to the maximum in use), with the
+    query rows of a KV-cache sequence at key positions Lk - Lq + i."""
+    q = inputgen.bf16_bits_to_f32(w.q).astype(np.float64)
+    k = inputgen.bf16_bits_to_f32(w.k).astype(np.float64)
+    v = inputgen.bf16_bits_to_f32(w.v).astype(np.float64)
+    G, W = w.Hq // w.Hkv, w.window
+    bound = np.zeros((w.total_tokens, w.Hq, w.D))
+    for s_, Lq in enumerate(w.seqlens):
+        a = int(w.cu_seqlens[s_])
+        if w.cu_seqlens_k is not None:
+            ak, Lk = int(w.cu_seqlens_k[s_]), int(w.seqlens_k[s_])
+        else:
+            ak, Lk = a, Lq
+        pos = (Lk - Lq) + np.arange(Lq)
+        for h in range(w.Hq):
+            qh, kg, vg = q[a:a + Lq, h], k[ak:ak + Lk, h // G], np.abs(v[ak:ak + Lk, h // G])
+            # scores of the keys d = 0 .. W-1 back from each query (-inf before the start)
+            sc = np.full((W, Lq), -np.inf)
+            for d in range(W):
+                ok = pos - d >= 0
+                sc[d, ok] = w.scale * np.einsum("id,id->i", qh[ok], kg[pos[ok] - d])
+            m = np.maximum(sc.max(axis=0), w.sinks[h])
+            pr = np.exp(sc - m)
+            l = pr.sum(axis=0) + np.exp(w.sinks[h] - m)
+            acc = np.zeros((Lq, w.D))
+            for d in range(W):
+                ok = pos - d >= 0
+                acc[ok] += (pr[d, ok] / 256)[:, None] * vg[pos[ok] - d]
+            bound[a:a + Lq, h] = acc / l[:, None]
+    return bound
+
+
+@pytest.mark.parametrize("kvcache", [False, True])
 @pytest.mark.parametrize("window", [1, 2])
-def test_few_key_windows_within_the_rounding_bound(window):
+def test_few_key_windows_within_the_rounding_bound(window, kvcache):
     """With one or two keys per row the flat max tolerance is within a factor
     of the bf16 rounding of P itself: P is rounded to bf16 before PV (each p
     moves by at most p/256 relative to the maximum in use) and the output is
     rounded to bf16, so |out - exact| <= sum_j (p_j / 256)|v_j| / l + |out|
     2^-8 (+ fp32 noise); for |v| near 5 (the N(0,1) tail over 10^6 values)
     that passes 2e-2.  Every element is checked against that bound, the mean
-    against the flat 2e-3."""
-    w = inputgen.make([1536, 2049, 700], 32, 8, window=window, seed=40 + window)
+    against the flat 2e-3.  The KV-cache form puts the window at the end of
+    a longer key sequence (and a sequence whose keys start at its queries)."""
+    if kvcache:
+        w = inputgen.make_kvcache([2049, 128, 700], [2149, 828, 700], 8, 2, window=window,
+                                  seed=50 + window)
+    else:
+        w = inputgen.make([1536, 2049, 700], 32, 8, window=window, seed=40 + window)
     out, lse = parity.run_gpu(w)
     out = out.float().cpu().numpy().astype(np.float64)
     lse = lse.cpu().numpy().astype(np.float64)
     ro, rl, _ = oracle.run_workload(w)
-    q = inputgen.bf16_bits_to_f32(w.q).astype(np.float64)
-    k = inputgen.bf16_bits_to_f32(w.k).astype(np.float64)
-    v = inputgen.bf16_bits_to_f32(w.v).astype(np.float64)
-    G = w.Hq // w.Hkv
-    bound = np.zeros_like(ro)
-    for s_, L in enumerate(w.seqlens):
-        a = int(w.cu_seqlens[s_])
-        for h in range(w.Hq):
-            qh, kg, vg = q[a:a + L, h], k[a:a + L, h // G], np.abs(v[a:a + L, h // G])
-            # scores of key offsets d = 0 .. window-1 back from each query (-inf before the start)
-            sc = np.full((window, L), -np.inf)
-            for d in range(window):
-                sc[d, d:] = w.scale * np.einsum("id,id->i", qh[d:], kg[:L - d])
-            m = np.maximum(sc.max(axis=0), w.sinks[h])
-            pr = np.exp(sc - m)
-            l = pr.sum(axis=0) + np.exp(w.sinks[h] - m)
-            acc = np.zeros((L, w.D))
-            for d in range(window):
-                acc[d:] += (pr[d, d:] / 256)[:, None] * vg[:L - d]
-            bound[a:a + L, h] = acc / l[:, None]
+    bound = few_key_rounding_bound(w)
     err = np.abs(out - ro)
     worst = (err - bound - np.abs(ro) * 2.0 ** -8 - 1e-4).max()
-    print(f"W={window}: out max {err.max():.3g} mean {err.mean():.3g}, bound max {bound.max():.3g}, "
-          f"lse max {np.abs(lse - rl).max():.3g}")
+    print(f"W={window} kv={kvcache}: out max {err.max():.3g} mean {err.mean():.3g}, "
+          f"bound max {bound.max():.3g}, lse max {np.abs(lse - rl).max():.3g}")
     assert worst <= 0, f"rounding bound exceeded by {worst}"
     assert err.mean() <= 2e-3 and np.abs(lse - rl).max() <= 1e-3
 
