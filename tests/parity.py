@@ -87,3 +87,37 @@ def check_sampled(w: inputgen.Workload, n_rows=4096, label=None, d=None):
     # every output must be finite, not only the sampled rows
     assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all()), "non-finite rows"
     return compare(o, l, ro, rl, (label or w.name) + f" [{len(t)} rows]")
+
+
+def few_key_rounding_bound(w):
+    """sum_j (p_j / 256)|v_j| / l per output element for a window of a few
+    keys (the bf16 rounding of P, relative to the maximum in use), with the
+    query rows of a KV-cache sequence at key positions Lk - Lq + i."""
+    q = inputgen.bf16_bits_to_f32(w.q).astype(np.float64)
+    k = inputgen.bf16_bits_to_f32(w.k).astype(np.float64)
+    v = inputgen.bf16_bits_to_f32(w.v).astype(np.float64)
+    G, W = w.Hq // w.Hkv, w.window
+    bound = np.zeros((w.total_tokens, w.Hq, w.D))
+    for s_, Lq in enumerate(w.seqlens):
+        a = int(w.cu_seqlens[s_])
+        if w.cu_seqlens_k is not None:
+            ak, Lk = int(w.cu_seqlens_k[s_]), int(w.seqlens_k[s_])
+        else:
+            ak, Lk = a, Lq
+        pos = (Lk - Lq) + np.arange(Lq)
+        for h in range(w.Hq):
+            qh, kg, vg = q[a:a + Lq, h], k[ak:ak + Lk, h // G], np.abs(v[ak:ak + Lk, h // G])
+            # scores of the keys d = 0 .. W-1 back from each query (-inf before the start)
+            sc = np.full((W, Lq), -np.inf)
+            for d in range(W):
+                ok = pos - d >= 0
+                sc[d, ok] = w.scale * np.einsum("id,id->i", qh[ok], kg[pos[ok] - d])
+            m = np.maximum(sc.max(axis=0), w.sinks[h])
+            pr = np.exp(sc - m)
+            l = pr.sum(axis=0) + np.exp(w.sinks[h] - m)
+            acc = np.zeros((Lq, w.D))
+            for d in range(W):
+                ok = pos - d >= 0
+                acc[ok] += (pr[d, ok] / 256)[:, None] * vg[pos[ok] - d]
+            bound[a:a + Lq, h] = acc / l[:, None]
+    return bound

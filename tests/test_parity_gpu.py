@@ -53,40 +53,6 @@ def test_odd_group_mixes_one_and_two_tile_units(D, window):
     print(parity.check_sampled(w, n_rows=8192, label=f"G=5 D={D} W={window}"))
 
 
-def few_key_rounding_bound(w):
-    """sum_j (p_j / 256)|v_j| / l per output element for a window of a few
-    keys (the bf16 rounding of P, relative to the maximum in use), with the
-    query rows of a KV-cache sequence at key positions Lk - Lq + i."""
-    q = inputgen.bf16_bits_to_f32(w.q).astype(np.float64)
-    k = inputgen.bf16_bits_to_f32(w.k).astype(np.float64)
-    v = inputgen.bf16_bits_to_f32(w.v).astype(np.float64)
-    G, W = w.Hq // w.Hkv, w.window
-    bound = np.zeros((w.total_tokens, w.Hq, w.D))
-    for s_, Lq in enumerate(w.seqlens):
-        a = int(w.cu_seqlens[s_])
-        if w.cu_seqlens_k is not None:
-            ak, Lk = int(w.cu_seqlens_k[s_]), int(w.seqlens_k[s_])
-        else:
-            ak, Lk = a, Lq
-        pos = (Lk - Lq) + np.arange(Lq)
-        for h in range(w.Hq):
-            qh, kg, vg = q[a:a + Lq, h], k[ak:ak + Lk, h // G], np.abs(v[ak:ak + Lk, h // G])
-            # scores of the keys d = 0 .. W-1 back from each query (-inf before the start)
-            sc = np.full((W, Lq), -np.inf)
-            for d in range(W):
-                ok = pos - d >= 0
-                sc[d, ok] = w.scale * np.einsum("id,id->i", qh[ok], kg[pos[ok] - d])
-            m = np.maximum(sc.max(axis=0), w.sinks[h])
-            pr = np.exp(sc - m)
-            l = pr.sum(axis=0) + np.exp(w.sinks[h] - m)
-            acc = np.zeros((Lq, w.D))
-            for d in range(W):
-                ok = pos - d >= 0
-                acc[ok] += (pr[d, ok] / 256)[:, None] * vg[pos[ok] - d]
-            bound[a:a + Lq, h] = acc / l[:, None]
-    return bound
-
-
 @pytest.mark.parametrize("kvcache", [False, True])
 @pytest.mark.parametrize("window", [1, 2])
 def test_few_key_windows_within_the_rounding_bound(window, kvcache):
@@ -107,7 +73,7 @@ def test_few_key_windows_within_the_rounding_bound(window, kvcache):
     out = out.float().cpu().numpy().astype(np.float64)
     lse = lse.cpu().numpy().astype(np.float64)
     ro, rl, _ = oracle.run_workload(w)
-    bound = few_key_rounding_bound(w)
+    bound = parity.few_key_rounding_bound(w)
     err = np.abs(out - ro)
     worst = (err - bound - np.abs(ro) * 2.0 ** -8 - 1e-4).max()
     print(f"W={window} kv={kvcache}: out max {err.max():.3g} mean {err.mean():.3g}, "
