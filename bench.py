@@ -4,6 +4,12 @@ number through the C ABI with host buffers, and the CPU oracle as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...    # the CPU oracle as the reference arm
+  python bench.py ... --log runs.jsonl [--resume]
+
+--log appends the printed line to a file as well; with --resume a run whose
+(workload, seed, implementation, GPU count) the file already holds is not
+repeated: its logged line is printed again, so a sweep over workloads that
+was killed part way can be restarted with the same commands.
 
 One step = one tsk_mha_prefill call (scheduler pre-pass + attention kernel)
 over the whole workload, inputs resident in HBM.  L2 is flushed before every
@@ -246,7 +252,7 @@ def roofline_of(flops, alg_bytes, kernel_s, peaks, peak_src, fp8=False):
 def config_dict(w, ws):
     """The workload description both arms print (identical for the same run)."""
     kv = w.cu_seqlens_k is not None
-    return {"workload": w.name,
+    return {"workload": w.name, "seed": w.seed,
             "seqlens": w.seqlens if len(w.seqlens) <= 8 else f"{len(w.seqlens)} seqs",
             "total_tokens": w.total_tokens,
             "key_lengths": (w.seqlens_k if kv and len(w.seqlens_k) <= 8 else
@@ -256,6 +262,45 @@ def config_dict(w, ws):
             "inputs": "fp8 e4m3 (per-tensor scales)" if w.fp8 is not None else "bf16",
             "l2": "flushed before every timed GPU step (256 MB write, then 256 MB read)",
             "parallelism": "replicas" if ws > 1 else "single GPU"}
+
+
+def run_key(workload, seed, impl, n_gpus):
+    """What identifies a run in a --log file."""
+    return f"{workload}|{seed}|{impl}|{n_gpus}"
+
+
+def line_key(line):
+    c = line.get("config") or {}
+    return run_key(c.get("workload"), c.get("seed"), line.get("impl", "ours"), line.get("n_gpus"))
+
+
+def logged_line(path, key):
+    """The last line of the log `path` with this run key, or None.  Lines that
+    do not parse (one cut short by a killed run) are skipped."""
+    if not path or not os.path.exists(path):
+        return None
+    found = None
+    with open(path) as f:
+        for text in f:
+            text = text.strip()
+            if not text:
+                continue
+            try:
+                d = json.loads(text)
+            except ValueError:
+                continue
+            if isinstance(d, dict) and line_key(d) == key:
+                found = text
+    return found
+
+
+def emit(line, log=None):
+    """Print the result line (and append it to the log file, if any)."""
+    text = json.dumps(line)
+    print(text, flush=True)
+    if log:
+        with open(log, "a") as f:
+            f.write(text + "\n")
 
 
 def parity_stats(gpu_out, gpu_lse, ref_out, ref_lse):
@@ -301,7 +346,7 @@ def run_reference(args, ws, rank):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line, args.log)
     return 0
 
 
@@ -316,10 +361,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--log", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--resume", action="store_true",
+                    help="with --log: print the logged line of this run instead of repeating it")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     ws, rank, local = dist_env()
+    if args.resume and args.log:
+        done = logged_line(args.log, run_key(args.workload, args.seed, args.impl, ws))
+        if done is not None:
+            if rank == 0:
+                print(done, flush=True)
+            return 0
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo", init_method="env://")
@@ -547,7 +601,7 @@ def main():
             of="the timed run's output (last step) at the cpu_baseline's sampled rows, "
                "against the CPU oracle",
             tolerance={"out_max_abs": 2e-2, "out_mean_abs": 2e-3, "lse_max_abs": 1e-3})
-    print(json.dumps(line), flush=True)
+    emit(line, args.log)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

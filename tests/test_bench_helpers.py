@@ -96,3 +96,41 @@ def test_reference_arm_reports_its_measured_step_time_and_the_same_config():
     # a measured time (at most the process's wall time), not an extrapolation
     assert 0 < line["ms_per_step"] <= wall * 1e3
     assert line["ms_per_full_workload_extrapolated"] > 0
+
+
+def test_log_lookup_takes_the_last_matching_line_and_skips_broken_ones(tmp_path):
+    b = _bench()
+    log = tmp_path / "runs.jsonl"
+    mk = lambda wl, seed, v, impl=None: dict(
+        {"config": {"workload": wl, "seed": seed}, "n_gpus": 1, "value": v},
+        **({"impl": impl} if impl else {}))
+    lines = [json.dumps(mk("a", 0, 1.0)), '{"config": {"workload": "a", "se',  # cut short
+             json.dumps(mk("a", 1, 2.0)), json.dumps(mk("a", 0, 3.0, "reference")),
+             json.dumps(mk("a", 0, 4.0)), ""]
+    log.write_text("\n".join(lines))
+    got = b.logged_line(str(log), b.run_key("a", 0, "ours", 1))
+    assert json.loads(got)["value"] == 4.0
+    assert json.loads(b.logged_line(str(log), b.run_key("a", 0, "reference", 1)))["value"] == 3.0
+    assert b.logged_line(str(log), b.run_key("a", 0, "ours", 2)) is None
+    assert b.logged_line(str(log), b.run_key("b", 0, "ours", 1)) is None
+    assert b.logged_line(str(tmp_path / "absent.jsonl"), b.run_key("a", 0, "ours", 1)) is None
+
+
+def test_resume_prints_the_logged_line_without_running_again(tmp_path):
+    import subprocess
+    import sys
+    log = tmp_path / "runs.jsonl"
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+           "--workload", "tiny_1x256_h4kv1", "--steps", "1", "--warmup", "3",
+           "--log", str(log), "--resume"]
+    first = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert first.returncode == 0, first.stderr
+    assert len(log.read_text().splitlines()) == 1
+    again = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert again.returncode == 0, again.stderr
+    assert again.stdout.strip().splitlines()[-1] == first.stdout.strip().splitlines()[-1]
+    assert len(log.read_text().splitlines()) == 1  # nothing appended, nothing rerun
+    other = subprocess.run(cmd + ["--seed", "1"], capture_output=True, text=True, timeout=300)
+    assert other.returncode == 0, other.stderr
+    assert json.loads(other.stdout.strip().splitlines()[-1])["config"]["seed"] == 1
+    assert len(log.read_text().splitlines()) == 2
