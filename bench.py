@@ -4,7 +4,7 @@ number through the C ABI with host buffers, and the CPU oracle as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...    # the CPU oracle as the reference arm
-  python bench.py ... --log runs.jsonl [--resume]
+  python bench.py ... --log runs.jsonl [--resume] [--sample-rows N]
 
 --log appends the printed line to a file as well; with --resume a run whose
 (workload, seed, implementation, GPU count) the file already holds is not
@@ -158,10 +158,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_rate(w, seconds_target, seed_stream=77, keep=None):
+def oracle_rate(w, seconds_target, seed_stream=77, keep=None, rows=0):
     """Times the CPU oracle on a uniform sample of (token, head) rows of `w`
-    sized for about `seconds_target` of CPU work.  Returns (flop/s, rows,
-    seconds, threads, flops)."""
+    sized for about `seconds_target` of CPU work (or of `rows` rows, if
+    given).  Returns (flop/s, rows, seconds, threads, flops)."""
     import oracle
     G = w.Hq // w.Hkv
     T = w.total_tokens
@@ -178,12 +178,15 @@ def oracle_rate(w, seconds_target, seed_stream=77, keep=None):
         nk = pos + 1 if w.window <= 0 else np.minimum(pos + 1, w.window)
         return t, h, float(4.0 * w.D * nk.sum())
 
-    n = 2048
-    t, h, fl = rows_flops(n)
-    t0 = time.perf_counter()
-    _, _, thr = oracle.run_workload(w, rows=(t, h))
-    dt = time.perf_counter() - t0
-    n2 = int(min(4_000_000, max(n, n * seconds_target / max(dt, 1e-3))))
+    if rows > 0:
+        n2 = int(rows)
+    else:
+        n = 2048
+        t, h, fl = rows_flops(n)
+        t0 = time.perf_counter()
+        oracle.run_workload(w, rows=(t, h))
+        dt = time.perf_counter() - t0
+        n2 = int(min(4_000_000, max(n, n * seconds_target / max(dt, 1e-3))))
     t, h, fl = rows_flops(n2)
     t0 = time.perf_counter()
     ro, rl, thr = oracle.run_workload(w, rows=(t, h))
@@ -360,6 +363,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sample-rows", type=int, default=0,
+                    help="rows of the oracle sample that checks the output (default: sized "
+                         "by --cpu-seconds)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--log", default=None, help="also append the JSON line to this file")
     ap.add_argument("--resume", action="store_true",
@@ -587,7 +593,7 @@ def main():
         # rate is the baseline, and its values for those rows check the output
         # of the last timed step.
         keep = {}
-        r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds, keep=keep)
+        r, n, dt, thr, fl = oracle_rate(w, args.cpu_seconds, keep=keep, rows=args.sample_rows)
         line["cpu_baseline"] = {"value": r / 1e12, "unit": "TFLOP/s", "cores": thr,
                                 "kind": "oracle",
                                 "sample": f"{n} uniform (token, head) rows of {w.name} "

@@ -134,3 +134,12 @@ def test_resume_prints_the_logged_line_without_running_again(tmp_path):
     assert other.returncode == 0, other.stderr
     assert json.loads(other.stdout.strip().splitlines()[-1])["config"]["seed"] == 1
     assert len(log.read_text().splitlines()) == 2
+
+
+def test_oracle_sample_of_a_given_size():
+    import inputgen
+    b = _bench()
+    keep = {}
+    _, n, _, thr, fl = b.oracle_rate(inputgen.config("tiny_1x256_h4kv1"), 1.0, keep=keep, rows=300)
+    assert n == 300 and keep["out"].shape == (300, 64) and keep["lse"].shape == (300,)
+    assert thr >= 1 and fl > 0
