@@ -88,7 +88,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   bool ok = true;
   TSK_TL_DECL;
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
-  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+  for (int ku = 0, u = cx.unit(0); u < cx.total_units && ok; u = cx.unit(++ku)) {
     const Unit w = decode_unit<QS>(p, u);
     if (q_iter >= 1) ok = mbar_wait(cx.bar(kBarQEmpty), (q_iter - 1) & 1, 1, p, cx.abort);
     if (!ok) break;
@@ -175,7 +175,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   const uint32_t d_o = cx.tmem + kColO0 + 128 * t;
   const uint32_t a_p = d_s + kColP;
   const uint32_t q_addr = cx.sbase + kSmemQ + t * kTile;
-  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+  for (int ku = 0, u = cx.unit(0); u < cx.total_units && ok; u = cx.unit(++ku)) {
     const Unit w = decode_unit<QS>(p, u);
     if (t >= w.ntiles) {
       // Idle in the unit: follow its Q and K/V fills and release them with
@@ -279,7 +279,7 @@ __device__ __forceinline__ void role_softmax(const Ctx& cx, const AttnParams& p,
   uint32_t turn = 0;  // softmax steps taken in units with two query tiles
   bool ok = true;
   TSK_TL_DECL;
-  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+  for (int ku = 0, u = cx.unit(0); u < cx.total_units && ok; u = cx.unit(++ku)) {
     TSK_EV(7);
     int n_kv, kv_lo, diag0, pos;
     bool pair;  // two query tiles: their softmax steps alternate
@@ -532,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cx.tmem = *tmem_slot;
   cx.abort = smem_u32(const_cast<int*>(abort_flag));
   cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
+  cx.alternate = false;
 
   // Registers move from the producer/MMA warpgroup (96 each) to the softmax
   // warpgroups (200 each): 128 x 96 + 256 x 200 = 63,488 <= 384 x 168, the

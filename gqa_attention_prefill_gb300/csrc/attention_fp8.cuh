@@ -167,7 +167,7 @@ __device__ __forceinline__ void role_producer(const Ctx& cx, const CUtensorMap* 
   uint32_t q_iter = 0, kv_iter = 0;
   bool ok = true;
   if (p.debug_stall) ok = mbar_wait(cx.bar(kBarNever), 0, 99, p, cx.abort);
-  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+  for (int ku = 0, u = cx.unit(0); u < cx.total_units && ok; u = cx.unit(++ku)) {
     const Unit w = decode_unit(p, u);
     const int qb = q_iter & 1;
     if (q_iter >= 2) ok = mbar_wait(cx.bar(kBarQEmpty + qb), ((q_iter >> 1) & 1) ^ 1, 1, p, cx.abort);
@@ -216,7 +216,7 @@ __device__ __forceinline__ void role_mma(const Ctx& cx, const AttnParams& p, int
   const uint32_t d_s = cx.tmem + kColS0 + 128 * t;
   const uint32_t d_o = cx.tmem + kColO0 + 64 * t;
   const uint32_t a_p = cx.tmem + kColP0 + 64 * t;
-  for (int u = blockIdx.x; u < cx.total_units && ok; u += gridDim.x) {
+  for (int ku = 0, u = cx.unit(0); u < cx.total_units && ok; u = cx.unit(++ku)) {
     const Unit w = decode_unit(p, u);
     const int qb = q_iter & 1;
     ok = mbar_wait(cx.bar(kBarQFull + qb), (q_iter >> 1) & 1, 3, p, cx.abort);
@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cx.tmem = *tmem_slot;
   cx.abort = smem_u32(const_cast<int*>(abort_flag));
   cx.total_units = p.ws[kWsNTiles] * p.Hkv * p.HP;
+  cx.alternate = true;
 
   if (warp == 0 && lane == 0) fp8::role_producer(cx, &tmQ, &tmK, &tmV, p);
   else if (warp == 1 && lane == 0) fp8::role_mma(cx, p, 0);

@@ -45,8 +45,8 @@ def test_head_groupings(Hq, Hkv):
 @pytest.mark.parametrize("window", [0, 700])
 def test_odd_group_mixes_one_and_two_tile_units(D, window):
     """G = 5: every KV head has two head pairs and one single head, and with
-    the CTAs' stride over the units (152 = 2 mod 3) each CTA alternates units
-    with one and two query tiles, so the idle tile's issuer and softmax warps
+    152 CTAs (2 mod 3) taking the units in rounds each CTA mixes units with
+    one and two query tiles, so the idle tile's issuer and softmax warps
     follow and release fills between present units many times per CTA."""
     w = inputgen.make([1536, 2000, 700, 129], 40, 8, D=D, window=window,
                       scale=D ** -0.5, seed=D + window)
